@@ -1,0 +1,211 @@
+/*
+ * tq.h — C ABI of libtq: TurboQuant KV-cache quantisation over a paged cache,
+ * written for NVIDIA GB300 (sm_103a).
+ *
+ * The method restated here comes from these pages:
+ *   [vLLM-TQ]  "vLLM 源码完全拆解(十九):TurboQuant KV Cache 量化——Hadamard 旋转、
+ *              Lloyd-Max 标量量化与分页缓存内核" (pinghaoyang.com.cn)
+ *   [TQ-intro] "vLLM TurboQuant 介绍:极低比特 KV Cache 量化" (beaiera.top)
+ *   [NVFP4-TQ] "NVIDIA KV Cache 量化中的 NVFP4 与 TurboQuant" (moonnryan.github.io)
+ *
+ * Two hot operations:
+ *   tq_store   per (token, KV head): L2 norm, normalised Walsh-Hadamard
+ *              rotation, Lloyd-Max bucketize, norm-correction fold, bit-pack
+ *              of the K indices (or an e4m3 cast for FP8 keys), asymmetric
+ *              uniform quantisation of V, and one slot written into the paged
+ *              cache through slot_mapping.
+ *   tq_decode  attention for one query token per sequence read straight from
+ *              the packed cache: split-K over partitions of the sequence with
+ *              an online softmax, then an LSE-weighted reduce. No 16-bit copy
+ *              of the cache is ever materialised.
+ *
+ * Conventions shared by every entry point
+ *   - Ownership: the caller owns every buffer. The library allocates nothing,
+ *     keeps no global state, never synchronises the stream and only enqueues
+ *     kernels on the given stream (NULL = the legacy default stream).
+ *   - Pointers documented "device" must be CUDA device memory of the current
+ *     device; "host" pointers are plain CPU memory read during the call.
+ *   - Errors detectable on the host return a negative tq_status before any
+ *     launch. A launch failure returns TQ_ERR_CUDA. Data-dependent problems
+ *     (a slot or block id out of range, a sequence longer than its block-table
+ *     row) never trap: the offending item is skipped and a bit is OR-ed into
+ *     the optional device status word (TQ_DEV_* below).
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st* tq_stream_t;
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = -1,        /* null pointer, bad size or count */
+  TQ_ERR_UNSUPPORTED = -2,        /* shape or preset this build does not run */
+  TQ_ERR_MISALIGNED = -3,         /* a pointer breaks its alignment rule */
+  TQ_ERR_WORKSPACE_TOO_SMALL = -4,
+  TQ_ERR_CUDA = -5                /* a kernel launch failed */
+} tq_status;
+
+/* Presets: [vLLM-TQ] section "TurboQuant 在 vLLM 中的位置", subsection
+ * "四个预设对应什么" (TQ_PRESETS). */
+typedef enum {
+  TQ_PRESET_K8V4 = 0,     /* K: e4m3, no rotation, no norm; V: 4-bit        */
+  TQ_PRESET_4BIT_NC = 1,  /* K: 4-bit Lloyd-Max + norm correction; V: 4-bit */
+  TQ_PRESET_K3V4_NC = 2,  /* K: 3-bit Lloyd-Max + norm correction; V: 4-bit */
+  TQ_PRESET_3BIT_NC = 3   /* K: 3-bit + norm correction; V: 3-bit           */
+} tq_preset;
+
+typedef enum { TQ_DTYPE_F16 = 0, TQ_DTYPE_BF16 = 1, TQ_DTYPE_F32 = 2 } tq_dtype;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define TQ_DEV_SLOT_OUT_OF_RANGE  1u  /* store: slot // block_size >= num_blocks   */
+#define TQ_DEV_BLOCK_OUT_OF_RANGE 2u  /* decode: block id < 0 or >= num_blocks     */
+#define TQ_DEV_SEQ_TOO_LONG       4u  /* decode: seq_len > max_seq_len or > row cap */
+
+/* Problem description shared by store and decode. */
+typedef struct {
+  int preset;            /* tq_preset                                        */
+  int head_dim;          /* d; this build runs d = 128                        */
+  int block_size;        /* tokens per cache block: 16, 32, 64 or 128         */
+  int num_q_heads;       /* n_q (decode)                                      */
+  int num_kv_heads;      /* n_kv; n_q % n_kv == 0 and n_q / n_kv <= 8         */
+  int partition_tokens;  /* split-K partition length, a multiple of 16 in
+                            [16, 65536]; 0 selects 512                         */
+} tq_config;
+
+/* Byte layout of the paged cache (this library's ABI).
+ *
+ *   cache[num_blocks][n_kv][block_size / 16][tile_bytes]
+ *
+ * A tile holds 16 consecutive positions of one KV head, as separate regions:
+ *   k_off     16 rows x k_row_bytes: the key's LSB-first index stream (bit
+ *             b*i + j is bit j of index i; [vLLM-TQ] "位打包") or its e4m3 bytes
+ *   v_off     16 x v_row_bytes: value index streams, taken in token pairs
+ *             (2p, 2p+1) whose streams are interleaved in 16-bit words: word i
+ *             of token 2p+j is at v_off + p*2*v_row_bytes + 4*i + 2*j
+ *   knorm_off 16 x fp16 stored key norms (-1 for FP8 keys)
+ *   vscale_off, vzero_off   16 x fp16 value scales and zero points
+ * so tile_bytes = 16 * slot_bytes and block_bytes = block_size * n_kv *
+ * slot_bytes, the page size of [vLLM-TQ] "页内寻址:一页多少字节". Position p of
+ * sequence b is in block block_table[b][p / block_size], row p % block_size.
+ * Every region starts on a 16-byte boundary, so the kernels use 16-byte loads.
+ */
+typedef struct {
+  int key_bits;           /* 3 or 4, or 8 for e4m3 keys                   */
+  int value_bits;         /* 3 or 4                                        */
+  int key_fp8;
+  int norm_correction;
+  int key_packed_bytes;   /* per token, pages' key_packed_size             */
+  int value_packed_bytes; /* per token, pages' value_packed_size           */
+  int slot_bytes;         /* key_packed_bytes + value_packed_bytes         */
+  int tile_tokens;        /* 16                                            */
+  int tile_bytes;
+  int k_off, k_row_bytes;
+  int v_off, v_row_bytes;
+  int knorm_off, vscale_off, vzero_off;
+  long long block_bytes;
+} tq_layout;
+
+/* Lloyd-Max codebook for N(0, 1/d): [vLLM-TQ] section "Lloyd-Max 量化器".
+ * centroids ascending (num_levels = 2^bits of them), exactly antisymmetric,
+ * fp32; midpoints[i] = fp32((c[i] + c[i+1]) / 2), the decision boundaries the
+ * store compares against (a coordinate equal to a midpoint goes up). */
+typedef struct {
+  int head_dim;
+  int bits;
+  int num_levels;
+  float centroids[16];
+  float midpoints[15];
+} tq_codebook;
+
+/* Host. Solve the Lloyd-Max conditions for N(0, 1/head_dim) with `bits`
+ * (1..4) levels: closed-form Gaussian conditional means iterated from the
+ * uniform start on [-3.5 sigma, 3.5 sigma] to a 1e-13 change, symmetrised,
+ * rounded to fp32. Deterministic. out: host, written on TQ_OK. */
+tq_status tq_build_codebook(int head_dim, int bits, tq_codebook* out);
+
+/* Host. Fill *out with the cache layout of cfg (see tq_layout). Returns
+ * TQ_ERR_UNSUPPORTED for shapes the kernels do not run. */
+tq_status tq_layout_for(const tq_config* cfg, tq_layout* out);
+
+/* Device. Quantise and write num_tokens tokens into the cache.
+ *   cfg, cb       host; cb must be tq_build_codebook(d, key_bits) (ignored
+ *                 for TQ_PRESET_K8V4, may then be NULL)
+ *   key, value    device, [num_tokens][n_kv][d] contiguous, in_dtype f16 or
+ *                 bf16, 16-byte aligned
+ *   slot_mapping  device int64 [num_tokens]; slot < 0 writes nothing
+ *                 ([vLLM-TQ] "融合 kernel 的骨架"); slot s goes to block
+ *                 s / block_size, row s % block_size
+ *   cache         device, num_blocks * block_bytes bytes, 16-byte aligned
+ *   dev_status    device uint32 or NULL
+ * num_tokens == 0 is a no-op. Two tokens mapped to one slot race. */
+tq_status tq_store(const tq_config* cfg, const tq_codebook* cb,
+                   const void* key, const void* value, int in_dtype,
+                   long long num_tokens, const long long* slot_mapping,
+                   void* cache, long long num_blocks,
+                   unsigned int* dev_status, tq_stream_t stream);
+
+/* Bytes of decode workspace for `batch` sequences of at most max_seq_len
+ * tokens: split-K partials, [batch][n_q][P][d] fp32 plus [batch][n_q][P] fp32
+ * log2-sum-exp, P = ceil(max_seq_len / partition_tokens)
+ * ([vLLM-TQ] "精度与性能", subsection "内存:workspace 预分配"). 0 on bad input. */
+size_t tq_decode_workspace_size(const tq_config* cfg, int batch, int max_seq_len);
+
+/* Device. out[b][h][:] = softmax_p(scale * q[b][h] . k_p) @ v_p over the
+ * seq_lens[b] cached positions of sequence b, query head h reading KV head
+ * h / (n_q / n_kv). Keys and values are read from the packed cache; the query
+ * is rotated once ([vLLM-TQ] "读取内核", "分数计算:FP8 K 与 MSE K 的两条路径").
+ *   q            device [batch][n_q][d], q_dtype f16 or bf16, 16-byte aligned
+ *   cache        device, as written by tq_store
+ *   block_table  device int32 [batch][bt_stride]
+ *   seq_lens     device int32 [batch], each <= max_seq_len and
+ *                <= bt_stride * block_size; 0 gives zeros
+ *   scale        <= 0 selects 1/sqrt(d)
+ *   out          device [batch][n_q][d] of out_dtype (f16, bf16 or f32),
+ *                16-byte aligned
+ *   workspace    device, >= tq_decode_workspace_size bytes, 16-byte aligned;
+ *                its contents need no initialisation
+ * Launches the split-K kernel then the reduce kernel on `stream`. */
+tq_status tq_decode(const tq_config* cfg, const tq_codebook* cb,
+                    const void* q, int q_dtype,
+                    const void* cache, long long num_blocks,
+                    const int* block_table, int bt_stride,
+                    const int* seq_lens, int batch, int max_seq_len, float scale,
+                    void* out, int out_dtype,
+                    void* workspace, size_t workspace_bytes,
+                    unsigned int* dev_status, tq_stream_t stream);
+
+/* The two stages of tq_decode, separately (same arguments and rules), for
+ * callers that time or overlap them. tq_decode_partials writes only the
+ * workspace; tq_decode_reduce reads it and writes out. */
+tq_status tq_decode_partials(const tq_config* cfg, const tq_codebook* cb,
+                             const void* q, int q_dtype,
+                             const void* cache, long long num_blocks,
+                             const int* block_table, int bt_stride,
+                             const int* seq_lens, int batch, int max_seq_len,
+                             float scale, void* workspace, size_t workspace_bytes,
+                             unsigned int* dev_status, tq_stream_t stream);
+tq_status tq_decode_reduce(const tq_config* cfg, const int* seq_lens, int batch,
+                           int max_seq_len, int bt_stride, void* out, int out_dtype,
+                           const void* workspace, size_t workspace_bytes,
+                           tq_stream_t stream);
+
+/* Host. Static description of a status code. */
+const char* tq_status_string(int status);
+
+/* Host. ABI version of this header (major * 100 + minor). */
+int tq_version(void);
+
+#define TQ_ABI_VERSION 100
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

@@ -1,0 +1,121 @@
+"""libtq on the host: load, exported symbols, host-side arithmetic, argument checks.
+
+No test here launches a kernel; every call either runs host code only or
+returns an error before reaching the GPU.
+"""
+
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import codebook as ocb
+from oracle import layout as olay
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tq():
+    from turboquant_paged_kv_gb300 import build
+    build.build()
+    import turboquant_paged_kv_gb300 as tq
+    return tq
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "tq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_]+\**\s+\**(tq_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(tq):
+    from turboquant_paged_kv_gb300 import _abi
+    declared = _declared_functions()
+    assert declared, "no declarations parsed"
+    lib = ctypes.CDLL(tq.lib_path())
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(_abi.EXPORTED) == declared
+    assert tq.tq_version() == 100
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("bits", [1, 2, 3, 4])
+def test_host_codebook_equals_oracle(tq, d, bits):
+    cb = tq.tq_build_codebook(d, bits)
+    n = 2 ** bits
+    assert cb.num_levels == n and cb.bits == bits and cb.head_dim == d
+    got = np.array(cb.centroids[:n], dtype=np.float32)
+    ref = ocb.codebook(d, bits)
+    assert np.array_equal(got, ref)
+    assert np.array_equal(np.array(cb.midpoints[: n - 1], dtype=np.float32), ocb.midpoints_fp32(ref))
+
+
+@pytest.mark.parametrize("preset", ["k8v4", "4bit_nc", "k3v4_nc"])
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+def test_layout_equals_oracle(tq, preset, bs):
+    cfg = tq.make_config(preset, 32, 8, block_size=bs)
+    got = tq.tq_layout_for(cfg)
+    ref = olay.tile_layout(olay.PRESETS[preset], 128, bs, 8)
+    key, value, slot, _ = olay.preset_slot_sizes(olay.PRESETS[preset], 128)
+    assert (got.key_packed_bytes, got.value_packed_bytes, got.slot_bytes) == (key, value, slot)
+    assert got.tile_bytes == ref.tile_bytes and got.block_bytes == ref.block_bytes
+    assert (got.k_off, got.k_row_bytes, got.v_off, got.v_row_bytes) == (ref.k_off, ref.kb, ref.v_off, ref.vb)
+    assert (got.knorm_off, got.vscale_off, got.vzero_off) == (ref.knorm_off, ref.vscale_off, ref.vzero_off)
+
+
+def test_unsupported_shapes(tq):
+    from turboquant_paged_kv_gb300 import _abi
+    lay = _abi.tq_layout()
+    lib = _abi.load()
+    for cfg, want in [(tq.make_config("4bit_nc", 8, 8, head_dim=96), _abi.TQ_ERR_UNSUPPORTED),
+                      (tq.make_config("4bit_nc", 8, 8, block_size=8), _abi.TQ_ERR_UNSUPPORTED),
+                      (tq.make_config(17, 8, 8), _abi.TQ_ERR_INVALID_ARG),
+                      (tq.make_config("3bit_nc", 8, 8), _abi.TQ_ERR_UNSUPPORTED)]:
+        assert lib.tq_layout_for(ctypes.byref(cfg), ctypes.byref(lay)) == want
+
+
+def test_workspace_size_matches_pages_example(tq, golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "memory.json")))["decode_workspace"]
+    cfg = tq.make_config("4bit_nc", g["num_heads"], 8, partition_tokens=512)
+    size = tq.tq_decode_workspace_size(cfg, g["max_num_reqs"], g["max_num_splits"] * 512)
+    # partials (d fp32) + one log-sum-exp per row: the pages' (d + 1) fp32 per row
+    rows = g["max_num_reqs"] * g["num_heads"] * g["max_num_splits"]
+    assert size == rows * (g["head_size"] + 1) * 4
+    assert abs(size - g["mid_o_bytes_approx"]) / g["mid_o_bytes_approx"] < 0.01
+    assert tq.tq_decode_workspace_size(cfg, -1, 10) == 0
+
+
+def test_host_argument_errors_return_before_launch(tq):
+    from turboquant_paged_kv_gb300 import _abi
+    lib = _abi.load()
+    cfg = tq.make_config("4bit_nc", 32, 8)
+    cb = tq.tq_build_codebook(128, 4)
+    cb3 = tq.tq_build_codebook(128, 3)
+    ok16 = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    st = lambda *a: lib.tq_store(ctypes.byref(cfg), *a)  # noqa: E731
+    # zero tokens is a no-op even with null pointers
+    assert st(ctypes.byref(cb), None, None, 1, 0, None, None, 0, None, None) == _abi.TQ_OK
+    assert st(ctypes.byref(cb), None, ok16, 1, 5, ok16, ok16, 4, None, None) == _abi.TQ_ERR_INVALID_ARG
+    assert st(ctypes.byref(cb), odd, ok16, 1, 5, ok16, ok16, 4, None, None) == _abi.TQ_ERR_MISALIGNED
+    assert st(ctypes.byref(cb3), ok16, ok16, 1, 5, ok16, ok16, 4, None, None) == _abi.TQ_ERR_INVALID_ARG
+    assert st(ctypes.byref(cb), ok16, ok16, 7, 5, ok16, ok16, 4, None, None) == _abi.TQ_ERR_INVALID_ARG
+    dec = lambda cfg_, ws_bytes, out=ok16, q=ok16: lib.tq_decode(  # noqa: E731
+        ctypes.byref(cfg_), ctypes.byref(cb), q, 1, ok16, 10, ok16, 4, ok16, 2, 64, 0.0, out, 2, ok16,
+        ws_bytes, None, None)
+    need = tq.tq_decode_workspace_size(cfg, 2, 64)
+    assert dec(cfg, need - 1) == _abi.TQ_ERR_WORKSPACE_TOO_SMALL
+    assert dec(cfg, need, out=odd) == _abi.TQ_ERR_MISALIGNED
+    assert dec(cfg, need, q=odd) == _abi.TQ_ERR_MISALIGNED
+    assert dec(cfg, need, q=None) == _abi.TQ_ERR_INVALID_ARG
+    wide = tq.make_config("4bit_nc", 32, 2)          # 16 query heads per KV head
+    assert dec(wide, 1 << 30) == _abi.TQ_ERR_UNSUPPORTED
+    uneven = tq.make_config("4bit_nc", 30, 8)
+    assert dec(uneven, 1 << 30) == _abi.TQ_ERR_INVALID_ARG
+    badpart = tq.make_config("4bit_nc", 32, 8, partition_tokens=40)
+    assert dec(badpart, 1 << 30) == _abi.TQ_ERR_INVALID_ARG

@@ -1,0 +1,122 @@
+"""TurboQuant paged KV cache for GB300: Python binding of libtq.
+
+Functions carry the C ABI's names (``include/tq.h``) and only marshal
+arguments: torch tensors become raw device pointers, the current CUDA stream
+becomes the launch stream, and a non-OK status raises ``TQError``. Every step
+of the store and the decode runs inside libtq's CUDA kernels; importing the
+package fails if the library is not built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import (PRESET_IDS, TQ_DEV_BLOCK_OUT_OF_RANGE, TQ_DEV_SEQ_TOO_LONG,  # noqa: F401
+                   TQ_DEV_SLOT_OUT_OF_RANGE, TQ_DTYPE_BF16, TQ_DTYPE_F16, TQ_DTYPE_F32,
+                   TQError, tq_codebook, tq_config, tq_layout)
+
+_LIB = _abi.load()
+
+_DTYPES = {torch.float16: TQ_DTYPE_F16, torch.bfloat16: TQ_DTYPE_BF16, torch.float32: TQ_DTYPE_F32}
+
+__all__ = ["make_config", "tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode",
+           "tq_decode_partials", "tq_decode_reduce", "tq_decode_workspace_size", "tq_status_string",
+           "tq_version", "TQError", "lib_path"]
+
+
+def lib_path() -> str:
+    return _abi.lib_path()
+
+
+def make_config(preset: str | int, num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
+                block_size: int = 16, partition_tokens: int = 0) -> tq_config:
+    pid = PRESET_IDS[preset] if isinstance(preset, str) else int(preset)
+    return tq_config(pid, head_dim, block_size, num_q_heads, num_kv_heads, partition_tokens)
+
+
+def tq_build_codebook(head_dim: int, bits: int) -> tq_codebook:
+    cb = tq_codebook()
+    _abi.check("tq_build_codebook", _LIB.tq_build_codebook(head_dim, bits, ctypes.byref(cb)))
+    return cb
+
+
+def tq_layout_for(cfg: tq_config) -> tq_layout:
+    lay = tq_layout()
+    _abi.check("tq_layout_for", _LIB.tq_layout_for(ctypes.byref(cfg), ctypes.byref(lay)))
+    return lay
+
+
+def tq_decode_workspace_size(cfg: tq_config, batch: int, max_seq_len: int) -> int:
+    return int(_LIB.tq_decode_workspace_size(ctypes.byref(cfg), batch, max_seq_len))
+
+
+def tq_status_string(status: int) -> str:
+    return _LIB.tq_status_string(status).decode()
+
+
+def tq_version() -> int:
+    return int(_LIB.tq_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _cb(cb):
+    return None if cb is None else ctypes.byref(cb)
+
+
+def tq_store(cfg: tq_config, cb, key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor,
+             cache: torch.Tensor, num_blocks: int | None = None, dev_status: torch.Tensor | None = None,
+             stream=None) -> None:
+    """key, value [N, n_kv, d] f16/bf16; slot_mapping [N] int64; cache uint8."""
+    lay = tq_layout_for(cfg)
+    if num_blocks is None:
+        num_blocks = cache.numel() // lay.block_bytes
+    _abi.check("tq_store", _LIB.tq_store(
+        ctypes.byref(cfg), _cb(cb), _ptr(key), _ptr(value), _DTYPES[key.dtype], key.shape[0],
+        _ptr(slot_mapping), _ptr(cache), num_blocks, _ptr(dev_status), _stream(stream)))
+
+
+def tq_decode(cfg: tq_config, cb, q: torch.Tensor, cache: torch.Tensor, block_table: torch.Tensor,
+              seq_lens: torch.Tensor, max_seq_len: int, out: torch.Tensor, workspace: torch.Tensor,
+              scale: float = 0.0, num_blocks: int | None = None, dev_status: torch.Tensor | None = None,
+              stream=None) -> None:
+    """q [B, n_q, d]; block_table [B, stride] int32; seq_lens [B] int32; out [B, n_q, d]."""
+    lay = tq_layout_for(cfg)
+    if num_blocks is None:
+        num_blocks = cache.numel() // lay.block_bytes
+    _abi.check("tq_decode", _LIB.tq_decode(
+        ctypes.byref(cfg), _cb(cb), _ptr(q), _DTYPES[q.dtype], _ptr(cache), num_blocks,
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, float(scale),
+        _ptr(out), _DTYPES[out.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream)))
+
+
+def tq_decode_partials(cfg: tq_config, cb, q: torch.Tensor, cache: torch.Tensor, block_table: torch.Tensor,
+                       seq_lens: torch.Tensor, max_seq_len: int, workspace: torch.Tensor, scale: float = 0.0,
+                       num_blocks: int | None = None, dev_status: torch.Tensor | None = None,
+                       stream=None) -> None:
+    lay = tq_layout_for(cfg)
+    if num_blocks is None:
+        num_blocks = cache.numel() // lay.block_bytes
+    _abi.check("tq_decode_partials", _LIB.tq_decode_partials(
+        ctypes.byref(cfg), _cb(cb), _ptr(q), _DTYPES[q.dtype], _ptr(cache), num_blocks,
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, float(scale),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)))
+
+
+def tq_decode_reduce(cfg: tq_config, seq_lens: torch.Tensor, batch: int, max_seq_len: int, bt_stride: int,
+                     out: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    _abi.check("tq_decode_reduce", _LIB.tq_decode_reduce(
+        ctypes.byref(cfg), _ptr(seq_lens), batch, max_seq_len, bt_stride, _ptr(out), _DTYPES[out.dtype],
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -3,8 +3,8 @@
 Functions carry the C ABI's names (``include/tq.h``) and only marshal
 arguments: torch tensors become raw device pointers, the current CUDA stream
 becomes the launch stream, and a non-OK status raises ``TQError``. Every step
-of the store and the decode runs inside libtq's CUDA kernels; importing the
-package fails if the library is not built.
+of the store and the decode runs inside libtq's CUDA kernels; the first call
+raises ImportError if the library is not built (there is no fallback path).
 """
 
 from __future__ import annotations
@@ -18,7 +18,16 @@ from ._abi import (PRESET_IDS, TQ_DEV_BLOCK_OUT_OF_RANGE, TQ_DEV_SEQ_TOO_LONG,  
                    TQ_DEV_SLOT_OUT_OF_RANGE, TQ_DTYPE_BF16, TQ_DTYPE_F16, TQ_DTYPE_F32,
                    TQError, tq_codebook, tq_config, tq_layout)
 
-_LIB = _abi.load()
+
+
+class _LazyLib:
+    """libtq.so, loaded on first use (raises ImportError if it is not built)."""
+
+    def __getattr__(self, name):
+        return getattr(_abi.load(), name)
+
+
+_LIB = _LazyLib()
 
 _DTYPES = {torch.float16: TQ_DTYPE_F16, torch.bfloat16: TQ_DTYPE_BF16, torch.float32: TQ_DTYPE_F32}
 

@@ -67,6 +67,8 @@ typedef enum { TQ_DTYPE_F16 = 0, TQ_DTYPE_BF16 = 1, TQ_DTYPE_F32 = 2 } tq_dtype;
 #define TQ_DEV_SLOT_OUT_OF_RANGE  1u  /* store: slot // block_size >= num_blocks   */
 #define TQ_DEV_BLOCK_OUT_OF_RANGE 2u  /* decode: block id < 0 or >= num_blocks     */
 #define TQ_DEV_SEQ_TOO_LONG       4u  /* decode: seq_len > max_seq_len or > row cap */
+#define TQ_DEV_TIMEOUT            8u  /* decode: a bounded wait on a copy expired, or the
+                                         launch's shared-memory plan did not fit */
 
 /* Problem description shared by store and decode. */
 typedef struct {
@@ -75,8 +77,10 @@ typedef struct {
   int block_size;        /* tokens per cache block: 16, 32, 64 or 128         */
   int num_q_heads;       /* n_q (decode)                                      */
   int num_kv_heads;      /* n_kv; n_q % n_kv == 0 and n_q / n_kv <= 8         */
-  int partition_tokens;  /* split-K partition length, a multiple of 16 in
-                            [16, 65536]; 0 selects 512                         */
+  int partition_tokens;  /* 0: a partial covers at most one whole sequence of
+                            one KV head; > 0 (a multiple of 16): partials are
+                            also cut every partition_tokens positions. Work is
+                            split evenly over the GPU in either case.          */
 } tq_config;
 
 /* Byte layout of the paged cache (this library's ABI).
@@ -151,10 +155,15 @@ tq_status tq_store(const tq_config* cfg, const tq_codebook* cb,
                    void* cache, long long num_blocks,
                    unsigned int* dev_status, tq_stream_t stream);
 
-/* Bytes of decode workspace for `batch` sequences of at most max_seq_len
- * tokens: split-K partials, [batch][n_q][P][d] fp32 plus [batch][n_q][P] fp32
- * log2-sum-exp, P = ceil(max_seq_len / partition_tokens)
- * ([vLLM-TQ] "精度与性能", subsection "内存:workspace 预分配"). 0 on bad input. */
+/* Host. Bytes of decode workspace for `batch` sequences of at most
+ * max_seq_len tokens ([vLLM-TQ] "精度与性能", subsection "内存:workspace 预分配").
+ * The decode splits the tile line of all (sequence, KV head) pairs evenly over
+ * the warps of a persistent grid (at most 256 CTAs x 12 warps); each warp
+ * writes one partial per segment it touches. A partial holds (acc / l) fp32
+ * [d] and a log2-sum-exp fp32 for each of the n_q / n_kv query heads, and
+ * there are at most batch * n_kv * P + 3072 of them, P = 1 when
+ * partition_tokens is 0, else ceil(max_seq_len / partition_tokens).
+ * Independent of the device. 0 on bad input. */
 size_t tq_decode_workspace_size(const tq_config* cfg, int batch, int max_seq_len);
 
 /* Device. out[b][h][:] = softmax_p(scale * q[b][h] . k_p) @ v_p over the

@@ -41,7 +41,7 @@ def oracle_case(name, **over):
 def gpu_decode(tq, w, inp, cache_np, out_dtype=torch.float32, partition_tokens=None, seq_lens=None,
                block_table=None, q=None, status=None, max_seq_len=None):
     cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size,
-                         partition_tokens=partition_tokens or w.partition_tokens)
+                         partition_tokens=w.partition_tokens if partition_tokens is None else partition_tokens)
     cb = None if w.preset == "k8v4" else tq.tq_build_codebook(w.d, 3 if w.preset.startswith("k3") else 4)
     cache = torch.from_numpy(cache_np).cuda()
     lens = (inp.seq_lens if seq_lens is None else seq_lens).cuda()
@@ -82,7 +82,7 @@ def test_decode_fp16_query(tq):
     assert_decode_close(got, ref16, torch.float32)
 
 
-@pytest.mark.parametrize("pt", [16, 48, 128, 512, 4096])
+@pytest.mark.parametrize("pt", [0, 16, 48, 128, 512, 4096])
 def test_decode_partition_invariance(tq, pt):
     w, inp, oc, q, ref = oracle_case("gqa_small")
     got = gpu_decode(tq, w, inp, oc.cache, partition_tokens=pt)

@@ -32,6 +32,7 @@ TQ_DTYPE_F32 = 2
 TQ_DEV_SLOT_OUT_OF_RANGE = 1
 TQ_DEV_BLOCK_OUT_OF_RANGE = 2
 TQ_DEV_SEQ_TOO_LONG = 4
+TQ_DEV_TIMEOUT = 8
 
 # every function tq.h declares (checked by the ABI tests)
 EXPORTED = ("tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode_workspace_size",

@@ -121,18 +121,6 @@ tq_status tq_build_codebook(int head_dim, int bits, tq_codebook* out) {
 
 tq_status tq_layout_for(const tq_config* cfg, tq_layout* out) { return tq::make_layout(cfg, out); }
 
-size_t tq_decode_workspace_size(const tq_config* cfg, int batch, int max_seq_len) {
-  tq_layout L;
-  if (!cfg || batch < 0 || max_seq_len < 0 || tq::make_layout(cfg, &L) != TQ_OK) return 0;
-  const int pt = tq::effective_partition(cfg);
-  if (pt % tq::kTileTokens || pt < 16 || pt > 65536) return 0;
-  const long long parts = (static_cast<long long>(max_seq_len) + pt - 1) / pt;
-  const long long rows = static_cast<long long>(batch) * cfg->num_q_heads * (parts > 0 ? parts : 1);
-  // partial outputs [rows][d] fp32, then the per-row log2-sum-exp, rounded to 16 B
-  long long bytes = rows * cfg->head_dim * 4 + ((rows * 4 + 15) / 16) * 16;
-  return static_cast<size_t>(bytes > 16 ? bytes : 16);
-}
-
 const char* tq_status_string(int status) {
   switch (status) {
     case TQ_OK: return "ok";

@@ -91,8 +91,10 @@ typedef struct {
  *   k_off     16 rows x k_row_bytes: the key's LSB-first index stream (bit
  *             b*i + j is bit j of index i; [vLLM-TQ] "位打包") or its e4m3 bytes
  *   v_off     16 x v_row_bytes: value index streams, taken in token pairs
- *             (2p, 2p+1) whose streams are interleaved in 16-bit words: word i
- *             of token 2p+j is at v_off + p*2*v_row_bytes + 4*i + 2*j
+ *             (2p, 2p+1) whose streams are interleaved in 16-bit words, four
+ *             words per token in each 16-byte group: word i of token 2p+j is
+ *             at v_off + 2p*v_row_bytes + 16*((i >> 2) ^ x) + 4*(i & 3) + 2j,
+ *             x = 2*(p & 3) when v_row_bytes % 64 == 0 (a bank swizzle), else 0
  *   knorm_off 16 x fp16 stored key norms (-1 for FP8 keys)
  *   vscale_off, vzero_off   16 x fp16 value scales and zero points
  * so tile_bytes = 16 * slot_bytes and block_bytes = block_size * n_kv *
@@ -158,10 +160,10 @@ tq_status tq_store(const tq_config* cfg, const tq_codebook* cb,
 /* Host. Bytes of decode workspace for `batch` sequences of at most
  * max_seq_len tokens ([vLLM-TQ] "精度与性能", subsection "内存:workspace 预分配").
  * The decode splits the tile line of all (sequence, KV head) pairs evenly over
- * the warps of a persistent grid (at most 256 CTAs x 12 warps); each warp
+ * the warps of a persistent grid (at most 256 CTAs x 16 warps); each warp
  * writes one partial per segment it touches. A partial holds (acc / l) fp32
  * [d] and a log2-sum-exp fp32 for each of the n_q / n_kv query heads, and
- * there are at most batch * n_kv * P + 3072 of them, P = 1 when
+ * there are at most batch * n_kv * P + 4096 of them, P = 1 when
  * partition_tokens is 0, else ceil(max_seq_len / partition_tokens).
  * Independent of the device. 0 on bad input. */
 size_t tq_decode_workspace_size(const tq_config* cfg, int batch, int max_seq_len);

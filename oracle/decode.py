@@ -28,7 +28,7 @@ import math
 import numpy as np
 
 from . import numerics, rotation
-from .layout import Preset, TileLayout, TILE_TOKENS
+from .layout import Preset, TileLayout, TILE_TOKENS, v_word_offset
 from .store import unpack_bits
 
 __all__ = ["read_positions", "dequantized_values", "decode"]
@@ -56,7 +56,7 @@ def read_positions(cache: np.ndarray, layout: TileLayout, blocks: np.ndarray,
     kaddr = (base + layout.k_off + r * layout.kb)[:, None] + np.arange(layout.kb)[None, :]
     kbytes = cache[kaddr]
     wi = np.arange(layout.vb // 2)[None, :]
-    vaddr = (base + layout.v_off + pair * 2 * layout.vb + 2 * j)[:, None] + 4 * wi
+    vaddr = (base + layout.v_off)[:, None] + v_word_offset(layout.vb, pair[:, None], wi, j[:, None])
     vbytes = np.empty((len(blocks), layout.vb), dtype=np.uint8)
     vbytes[:, 0::2] = cache[vaddr]
     vbytes[:, 1::2] = cache[vaddr + 1]

@@ -21,8 +21,12 @@ A tile holds 16 consecutive token positions of one KV head. Inside a tile:
              token r's LSB-first index stream (or its e4m3 bytes).
   V region   16 x VB bytes        (VB = ceil(d*bv/8)); tokens are taken in
              pairs (2p, 2p+1) and the two LSB-first index streams of a pair
-             are interleaved in 16-bit words: word i of token 2p+j sits at
-             byte p*2*VB + 4*i + 2*j of the region.
+             are interleaved in 16-bit words, four words of each token per
+             16-byte group: word i of token 2p+j sits at byte
+             p*2*VB + 16*((i >> 2) ^ x) + 4*(i & 3) + 2*j of the region, with
+             the group swizzle x = 2*(p & 3) when VB is a multiple of 64 (so a
+             quarter warp reading group g of pairs c = 0..3 touches 8 distinct
+             16-byte bank groups) and x = 0 otherwise.
   K norms    16 x fp16            (only for index-coded keys)
   V scales   16 x fp16
   V zeros    16 x fp16
@@ -39,7 +43,8 @@ from __future__ import annotations
 import math
 from dataclasses import dataclass
 
-__all__ = ["PRESETS", "Preset", "TileLayout", "preset_slot_sizes", "tile_layout", "TILE_TOKENS"]
+__all__ = ["PRESETS", "Preset", "TileLayout", "preset_slot_sizes", "tile_layout", "TILE_TOKENS",
+           "v_word_offset"]
 
 TILE_TOKENS = 16
 
@@ -103,6 +108,12 @@ class TileLayout:
         """Byte offset of the tile holding (block, head, in-block offset)."""
         return ((block * self.n_kv + head) * self.tiles_per_block
                 + offset // TILE_TOKENS) * self.tile_bytes
+
+
+def v_word_offset(vb: int, pair, word, j):
+    """Byte offset inside the V region of 16-bit word ``word`` of token 2*pair+j."""
+    swz = (2 * (pair & 3)) if vb % 64 == 0 else 0
+    return pair * 2 * vb + 16 * ((word >> 2) ^ swz) + 4 * (word & 3) + 2 * j
 
 
 def tile_layout(preset: Preset, d: int, block_size: int, n_kv: int) -> TileLayout:

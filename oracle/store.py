@@ -28,7 +28,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import numerics, rotation
-from .layout import Preset, TileLayout, TILE_TOKENS
+from .layout import Preset, TileLayout, TILE_TOKENS, v_word_offset
 
 __all__ = ["pack_bits", "unpack_bits", "quantize_keys", "quantize_values", "store"]
 
@@ -138,7 +138,7 @@ def store(k: np.ndarray, v: np.ndarray, slot_mapping: np.ndarray, cache: np.ndar
     # V region: pair-interleaved 16-bit words
     words = layout.vb // 2
     wi = np.arange(words)[None, :]
-    vaddr = base + layout.v_off + pair * 2 * layout.vb + 4 * wi + 2 * j
+    vaddr = base + layout.v_off + v_word_offset(layout.vb, pair, wi, j)
     vbytes = vinfo["packed"][rows]
     cache[vaddr] = vbytes[:, 0::2]
     cache[vaddr + 1] = vbytes[:, 1::2]

@@ -85,10 +85,10 @@ def test_workspace_size_matches_pages_example(tq, golden_dir):
     size = tq.tq_decode_workspace_size(cfg, g["max_num_reqs"], g["max_num_splits"] * 512)
     # one partial per (sequence, KV head, partition) -- (d + 1) fp32 for each of
     # the G query heads, the pages' mid_o -- plus one per warp of the largest
-    # persistent grid (256 CTAs x 12 warps), where a warp's range splits a segment
+    # persistent grid (256 CTAs x 16 warps), where a warp's range splits a segment
     group = g["num_heads"] // 8
     rows = g["max_num_reqs"] * g["num_heads"] * g["max_num_splits"]
-    extra = 256 * 12 * group * (g["head_size"] + 1) * 4
+    extra = 256 * 16 * group * (g["head_size"] + 1) * 4
     assert size == rows * (g["head_size"] + 1) * 4 + extra
     assert abs((size - extra) - g["mid_o_bytes_approx"]) / g["mid_o_bytes_approx"] < 0.01
     assert tq.tq_decode_workspace_size(cfg, -1, 10) == 0

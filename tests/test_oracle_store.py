@@ -116,13 +116,17 @@ def test_negative_and_out_of_range_slots_write_nothing():
 
 
 def test_value_pair_interleave_layout():
+    # tokens 6 and 7 form pair 3: their 16-bit words interleave, four words of
+    # each per 16-byte group, and group r is stored at slot r ^ (2 * (3 & 3))
     preset, lay, k, v, slots, cache, info, _ = _fill("4bit_nc", n_tok=2, n_kv=1, bs=16,
                                                      num_blocks=1, slots=np.array([6, 7]))
-    a = info["v"]["packed"][0]
-    b = info["v"]["packed"][1]
-    region = cache[lay.v_off + 3 * 2 * lay.vb: lay.v_off + 4 * 2 * lay.vb]
-    expect = np.stack([a.reshape(-1, 2), b.reshape(-1, 2)], axis=1).reshape(-1)
-    assert np.array_equal(region, expect)
+    a = info["v"]["packed"][0].reshape(8, 4, 2)   # [group][word][byte]
+    b = info["v"]["packed"][1].reshape(8, 4, 2)
+    region = cache[lay.v_off + 3 * 2 * lay.vb: lay.v_off + 4 * 2 * lay.vb].reshape(8, 4, 2, 2)
+    for r in range(8):
+        slot = r ^ 6
+        assert np.array_equal(region[slot, :, 0, :], a[r])
+        assert np.array_equal(region[slot, :, 1, :], b[r])
 
 
 def test_exact_tie_goes_to_upper_cell():

@@ -22,28 +22,41 @@
 //  segment + warp, which is unique because both sequences are monotone. Every
 //  warp does the same amount of work whatever the sequence lengths are.
 //
-//  Data movement. Each warp owns a ring of 4 tile buffers in shared memory fed
-//  by cp.async.bulk (one 2144-byte copy per tile at 4bit_nc, completion on an
-//  mbarrier) and two query buffers fed the same way; the ring runs ahead across
-//  segment boundaries. Block ids are read 32 at a time into a lane-indexed
+//  Data movement. Each warp owns a ring of 2 stages in shared memory, each a
+//  chunk of up to 4 consecutive tiles (64 positions) of one segment, fed by
+//  cp.async.bulk (one 2144-byte copy per tile at 4bit_nc, all completing on the
+//  stage's mbarrier), and two query buffers fed the same way; the ring runs
+//  ahead across segment boundaries. Per-chunk work (waits, the softmax max,
+//  the rescale vote) is amortised over 64 positions and the 4 tiles give the
+//  tensor pipe 4 independent accumulation chains. Block ids are read 32 at a time into a lane-indexed
 //  register window. Every mbarrier wait is bounded: on expiry the warp flags
 //  TQ_DEV_TIMEOUT, drains its own copies (bounded again) and stops.
 //
 //  Math. Both contractions run on tensor cores with mma.sync.m16n8k16 (f16 in,
-//  f32 accumulate), operands dequantised in registers:
-//    S^T[16 x 8 tok] = Q[16 x 16] . K^T. Rows g < 8 carry q_hi of query head g
-//      and rows 8 + g carry q_lo (q = q_hi + q_lo in fp16). The 16-wide k
-//      dimension holds 8 coordinates with centroid hi parts and the same 8
-//      with centroid lo parts: one 8-byte LUT entry per key byte (32 copies,
-//      one per lane, so lookups never conflict; the table is aligned so one
-//      PRMT forms the address) yields a whole B fragment, and the product is
-//      accurate to ~2^-22 relative (fp16 operands alone miss the 2e-3 gate).
-//    O^T[16 d x 8] = V^T[16 d x 16 tok] . P^T. Value codes are exact fp16
-//      integers; the store interleaves the 16-bit words of token pairs so one
-//      32-bit word gives four (token 2c, token 2c+1) operand pairs. Columns
+//  f32 accumulate; one such mma occupies a sub-partition's tensor pipe for
+//  about 8 cycles on GB300, so the layout wastes as few rows as possible):
+//    S[8 tok x 2 parts, 8] = K . Q^T. Rows g and 8 + g hold token g with the
+//      centroid hi and lo parts (c = c_hi + c_lo in fp16); one 8-byte LUT entry
+//      per key byte (32 copies, one per lane, so lookups never conflict; the
+//      table is aligned so one PRMT forms the address) is exactly the (row g,
+//      row 8 + g) operand pair, and the two rows are summed in the same lane.
+//      Columns hold q_hi of the G <= 4 query heads and q_lo of the same heads
+//      (q = q_hi + q_lo), so one mma per 16 coordinates covers all products to
+//      ~2^-22 relative (fp16 operands alone miss the 2e-3 output gate). For
+//      G > 4 the q_lo columns take a second mma.
+//    P^T reaches the B-operand layout through movmatrix.trans (the S layout has
+//      tokens in rows), one instruction per 8x8 block of fp16 hi or lo parts.
+//    O^T[16 d x 8] = V^T[16 d x 16 tok] . P^T. The store interleaves the 16-bit
+//      words of token pairs; masking a 32-bit word with 0x000F000F (or
+//      0x00F000F0) yields a half2 of the two tokens' codes as exact fp16
+//      subnormals (code * 2^-24, or code * 2^-20), so value operands cost one
+//      LOP3 per pair; the per-row power of two is removed at the end. The
+//      16-byte groups of the V region are XOR-swizzled by the pair index so
+//      these loads are free of bank conflicts. Columns
 //      carry hi and lo parts of p * scale; sum_p p * zero is kept on the side.
-//  Softmax in log2 units with a lazy rescale (the running max only moves when
-//  it grows by more than 2^8).
+//  Softmax in log2 units with a lazy rescale: the running max of a head only
+//  moves when it grows by more than 2^8, decided by a warp vote, so rescaling
+//  the accumulators is off the common path.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -59,12 +72,18 @@ namespace tq {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kWarps = 12;              // warps per CTA, one CTA per SM
-constexpr int kStages = 4;              // tile buffers per warp
+#ifndef TQ_DECODE_WARPS
+#define TQ_DECODE_WARPS 8
+#endif
+constexpr int kMaxWarps = TQ_DECODE_WARPS;   // warps per CTA (fewer when shared memory is short)
+constexpr int kChunk = 4;               // tiles per ring stage (64 tokens)
+constexpr int kStages = 2;              // ring stages per warp
 constexpr float kTau = 8.0f;            // lazy rescale threshold, log2 units
-constexpr uint32_t kWaitLimit = 1u << 21;
-constexpr int kQBufBytes = 8 * kD * 2;  // G <= 8 rows of 16-bit q
+constexpr uint32_t kWaitLimit = 1u << 16;
+constexpr uint32_t kSuspendNs = 20000;  // try_wait suspend hint: bound ~ kWaitLimit * 20 us
 constexpr int kMaxCtas = 256;           // grid cap; sizes the workspace without a device query
+constexpr int kRecordWarps = 16;        // warps per CTA the workspace allows for (>= kMaxWarps)
+static_assert(kMaxWarps <= kRecordWarps, "workspace sized for at most 16 warps per CTA");
 
 enum KeyMode { kMse4 = 4, kMse3 = 3, kFp8 = 8 };
 
@@ -82,7 +101,8 @@ struct DecodeArgs {
   int part_tiles;      // tiles per partition (0: whole sequence)
   int num_parts;       // partitions per (b, h) in the record index
   int max_seq_len, cap;
-  int tile_bytes, tile_stride, k_off, v_off, knorm_off, vscale_off, vzero_off;
+  int tile_bytes, stage_bytes, k_off, v_off, knorm_off, vscale_off, vzero_off;
+  int qbuf_bytes;      // G * d * 2
   int warp_bytes;      // per-warp shared buffer
   int dyn_bytes;
   float qscale;        // softmax scale * log2(e)
@@ -123,6 +143,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(a));
   return v;
 }
+__device__ __forceinline__ float lds_h2f(uint32_t a) {   // one fp16 -> float
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(a));
+  return __half2float(__ushort_as_half(v));
+}
 __device__ __forceinline__ void sts64(uint32_t a, uint2 v) {
   asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(a), "r"(v.x), "r"(v.y));
 }
@@ -133,12 +158,23 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_expect(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
 }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -184,9 +220,6 @@ __device__ __forceinline__ void split_half2(float x0, float x1, uint32_t& hi, ui
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = pack_half2(x0 - hf.x, x1 - hf.y);
 }
-__device__ __forceinline__ float2 half2_bits_to_float2(uint32_t w) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&w));
-}
 
 template <typename T>
 __device__ __forceinline__ void u2_to_f4(uint2 raw, float out[4]) {
@@ -221,23 +254,6 @@ __device__ __forceinline__ void flag(unsigned int* status, unsigned int bit) {
   if (status) atomicOr(status, bit);
 }
 
-__device__ __forceinline__ float lazy_update(float& m, float chunk_max) {
-  if (chunk_max > m + kTau) {
-    const float a = ex2(m - chunk_max);
-    m = chunk_max;
-    return a;
-  }
-  return 1.f;
-}
-
-// value codes -> half2 operands: token A in bits 0..15, token B in bits 16..31
-// of w; nibble j of each half, as exact integers (1024 + code, minus 1024).
-__device__ __forceinline__ uint32_t vpair(uint32_t w, int j) {
-  const uint32_t biased = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&biased), __half2half2(__ushort_as_half(0x6400)));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
@@ -265,42 +281,19 @@ __device__ void build_lut(uint32_t lut, const float* cent) {
   }
 }
 
-// S^T for one n-tile of 8 tokens, two independent accumulator chains.
+// Address of the LUT entry for k-step s (coordinates 32c + 2s, +1) of a key row
+// slice held in kq (this lane's bytes / bits of the row).
 template <int KMODE>
-__device__ __forceinline__ void qk_tile(float acc[2][4], const uint32_t qa[32], const uint4* kraw,
-                                        uint32_t lut_lane) {
+__device__ __forceinline__ uint32_t lut_addr(const uint4& kq, int s, uint32_t lut_lane) {
   if constexpr (KMODE == kMse4) {
-    const uint4 kq = kraw[0];
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      const uint32_t w = word_of(kq, s >> 2);
-      const uint32_t addr = __byte_perm(w, lut_lane, 0x7604u | ((s & 3) << 4));
-      const uint2 e = lds64(addr);
-      mma16816(acc[s & 1], qa[2 * s], qa[2 * s + 1], qa[2 * s], qa[2 * s + 1], e.x, e.y);
-    }
-  } else if constexpr (KMODE == kMse3) {
-    const uint4 kq = kraw[0];
-    const uint32_t w[3] = {kq.x, kq.y, kq.z};
-#pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      const int bit = 6 * s, wi = bit >> 5, sh = bit & 31;
-      uint32_t f;
-      if (sh <= 26) f = w[wi] >> sh;
-      else f = __funnelshift_r(w[wi], w[wi + 1], sh);
-      const uint32_t addr = ((f << 8) & 0x3F00u) | lut_lane;
-      const uint2 e = lds64(addr);
-      mma16816(acc[s & 1], qa[2 * s], qa[2 * s + 1], qa[2 * s], qa[2 * s + 1], e.x, e.y);
-    }
+    return __byte_perm(word_of(kq, s >> 2), lut_lane, 0x7604u | ((s & 3) << 4));
   } else {
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const uint32_t w = word_of(kraw[s >> 2], s & 3);
-      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3);
-      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
-      const uint32_t b0 = static_cast<uint32_t>(lo.x) | (static_cast<uint32_t>(lo.y) << 16);
-      const uint32_t b1 = static_cast<uint32_t>(hi.x) | (static_cast<uint32_t>(hi.y) << 16);
-      mma16816(acc[s & 1], qa[4 * s], qa[4 * s + 1], qa[4 * s + 2], qa[4 * s + 3], b0, b1);
-    }
+    const int bit = 6 * s, wi = bit >> 5, sh = bit & 31;
+    const uint32_t w0 = word_of(kq, wi);
+    uint32_t f;
+    if (sh <= 26) f = w0 >> sh;
+    else f = __funnelshift_r(w0, word_of(kq, wi + 1), sh);
+    return ((f << 8) & 0x3F00u) | lut_lane;
   }
 }
 
@@ -344,20 +337,23 @@ __device__ __forceinline__ bool walk_next(Walk& w, const DecodeArgs& a, int lane
   return false;
 }
 
-__device__ __forceinline__ long long segment_of(const Walk& w, const DecodeArgs& a) {
+__device__ __forceinline__ int segment_of(const Walk& w, const DecodeArgs& a) {
   const int p = a.part_tiles > 0 ? w.t / a.part_tiles : 0;
-  return (static_cast<long long>(w.b) * a.n_kv + w.h) * a.num_parts + p;
+  return (w.b * a.n_kv + w.h) * a.num_parts + p;
 }
 
 // ---------------------------------------------------------------- split kernel
 
+// One consumer step handles a chunk of up to kChunk consecutive tiles of one
+// segment, held in one ring stage.
 template <int KMODE, int GBIG, typename TQ>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+__global__ void __launch_bounds__(kMaxWarps * 32, 1)
 split_kernel(const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t s_dyn[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int g = lane >> 2;          // mma groupID: token row of B, query row of A
+  const int nwarp_cta = blockDim.x >> 5;
+  const int g = lane >> 2;          // mma groupID
   const int c = lane & 3;           // thread in group
   const int G = a.group;
 
@@ -380,9 +376,9 @@ split_kernel(const DecodeArgs a) {
   }
   if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent);
 
-  const uint32_t ring = my_base;                                  // kStages tiles
-  const uint32_t qbuf = ring + kStages * a.tile_stride;           // 2 query buffers
-  const uint32_t bars = qbuf + 2 * kQBufBytes;                    // kStages + 2 mbarriers
+  const uint32_t ring = my_base;                                  // kStages chunks
+  const uint32_t qbuf = ring + kStages * a.stage_bytes;           // 2 query buffers
+  const uint32_t bars = qbuf + 2 * a.qbuf_bytes;                  // kStages + 2 mbarriers
   if (lane == 0) {
     for (int i = 0; i < kStages + 2; ++i) mbar_init(bars + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -394,10 +390,9 @@ split_kernel(const DecodeArgs a) {
   const uint64_t policy = evict_first_policy();
 
   // ---- this warp's range of the tile line
-  const long long nwarps = static_cast<long long>(gridDim.x) * kWarps;
-  const long long wid = static_cast<long long>(blockIdx.x) * kWarps + warp;
-  // total tiles: n_kv * sum_b ceil(len_b / 16)
-  long long total = 0;
+  const long long nwarps = static_cast<long long>(gridDim.x) * nwarp_cta;
+  const int wid = blockIdx.x * nwarp_cta + warp;
+  long long total = 0;   // n_kv * sum_b ceil(len_b / 16)
   bool too_long = false;
   for (int b0 = 0; b0 < a.batch; b0 += 32) {
     const int j = b0 + lane;
@@ -407,18 +402,18 @@ split_kernel(const DecodeArgs a) {
       too_long |= raw > min(a.max_seq_len, a.cap);
       nt = (clamp_len(a, raw) + kTileTokens - 1) / kTileTokens;
     }
-    for (int o = 1; o < 32; o <<= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o);
+    for (int o_ = 1; o_ < 32; o_ <<= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o_);
     total += nt;
   }
   if (wid == 0 && __any_sync(0xffffffffu, too_long) && lane == 0) flag(a.status, TQ_DEV_SEQ_TOO_LONG);
   total *= a.n_kv;
-  const long long r0 = total * wid / nwarps, r1 = total * (wid + 1) / nwarps;
-  if (r0 >= r1) return;
+  const long long r0 = total * wid / nwarps;
+  const int ntiles = static_cast<int>(total * (wid + 1) / nwarps - r0);
+  if (ntiles <= 0) return;
 
-  // locate tile r0
-  Walk pw;   // producer cursor
+  Walk pw;   // producer cursor: locate tile r0
   {
-    long long acc = 0;   // tiles before sequence b, times n_kv
+    long long acc = 0;
     int b = 0;
     lens_fill(pw, a, 0, lane);
     for (;;) {
@@ -426,10 +421,10 @@ split_kernel(const DecodeArgs a) {
       const int nt = (len + kTileTokens - 1) / kTileTokens;
       const long long span = static_cast<long long>(nt) * a.n_kv;
       if (r0 < acc + span) {
-        const long long off = r0 - acc;
+        const int off = static_cast<int>(r0 - acc);
         pw.b = b; pw.len = len; pw.nt = nt;
-        pw.h = static_cast<int>(off / nt);
-        pw.t = static_cast<int>(off - static_cast<long long>(pw.h) * nt);
+        pw.h = off / nt;
+        pw.t = off - pw.h * nt;
         break;
       }
       acc += span;
@@ -438,326 +433,399 @@ split_kernel(const DecodeArgs a) {
   }
   Walk cw = pw;   // consumer cursor
 
-  // block-id window of the producer: lane j holds block (bid_base + j) of bid_b
-  int bid_b = -1, bid_base = 0, bid_reg = 0;
-
-  // ring bookkeeping
-  long long pi = r0, ci = r0;         // next tile to issue / to consume
-  unsigned tile_ok_bits = 0;          // per stage: block id was valid
-  long long p_seg = -1, c_seg = -1;   // segment of the last issued / consumed tile
-  int p_qslot = 1, c_qslot = 1;       // query buffer of that segment
-  unsigned q_uses0 = 0, q_uses1 = 0;  // phases consumed per query buffer
-  unsigned q_iss0 = 0, q_iss1 = 0;    // phases issued per query buffer
+  int bid_b = -1, bid_base = 0, bid_reg = 0;   // producer block-id window
+  int pi = 0, ci = 0;                           // tiles issued / consumed (relative to r0)
+  int p_stage = 0, c_stage = 0;
+  uint32_t c_phase = 0;                         // parity bit per stage, consumer side
+  uint32_t ok_bits = 0;                         // per stage, kChunk bits: tile copied
+  uint32_t stage_busy = 0;                      // per stage: issued, not yet consumed
+  int p_seg = -1, c_seg = -1;
+  int p_qslot = 1, c_qslot = 1;
+  uint32_t q_phase = 0, q_pending = 0;
   bool p_done = false, aborted = false;
 
-  // per-segment state
-  uint32_t qa[32];
-  float o[8][4];
-  float mrow = -INFINITY, mc0 = -INFINITY, mc1 = -INFINITY, lsum = 0.f, zsum = 0.f;
-  const auto col_row = [&](int n) -> int {
-    if (GBIG) return n < G ? n : 0;
-    return n < G ? n : (n < 2 * G ? n - G : 0);
-  };
-  const int rc0 = col_row(2 * c), rc1 = col_row(2 * c + 1);
+  uint32_t qb[GBIG ? 32 : 16];     // Q^T B operands (per k-step; GBIG: hi then lo)
+  float o[8][4];                   // O^T accumulators, rows d, cols n = 2c, 2c+1
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
 
-  while (ci < r1 && !aborted) {
-    // ---------------- producer: keep up to kStages tiles in flight; a new
-    // segment needs a free query buffer (the consumer must have begun the
-    // segment before it)
-    while (!p_done && pi - ci < kStages) {
-      const long long seg = segment_of(pw, a);
-      const bool new_seg = seg != p_seg;
-      if (new_seg && p_seg >= 0 && c_seg < p_seg) break;
-      if (new_seg) {
+  auto finalize = [&](int seg) {
+    float l_[2] = {l0, l1}, z_[2] = {z0, z1};
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int o_ = 4; o_ < 32; o_ <<= 1) {
+        l_[e] += __shfl_xor_sync(0xffffffffu, l_[e], o_);
+        z_[e] += __shfl_xor_sync(0xffffffffu, z_[e], o_);
+      }
+    const float mm[2] = {m0, m1};
+    const int rec = seg + wid;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int n = 2 * c + e;
+      const int pc = n + G;                      // lo column of head n (G <= 4)
+      const int src = 4 * g + ((pc >> 1) & 3);
+      const float inv = l_[e] > 0.f ? 1.f / l_[e] : 0.f;
+      float* dst = a.rec_o + (static_cast<long long>(rec) * G + (n < G ? n : 0)) * kD + 16 * g;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        float v0 = o[mt][e], v1 = o[mt][2 + e];
+        if (!GBIG) {
+          v0 += __shfl_sync(0xffffffffu, o[mt][pc & 1], src);
+          v1 += __shfl_sync(0xffffffffu, o[mt][2 + (pc & 1)], src);
+        }
+        // value operands carried code * 2^-24 (rows g) and code * 2^-20 (rows g + 8)
+        if (n < G)
+          *reinterpret_cast<float2*>(dst + 2 * mt) =
+              make_float2(fmaf(v0, 16777216.f, z_[e]) * inv, fmaf(v1, 1048576.f, z_[e]) * inv);
+      }
+      if (n < G && g == 0)
+        a.rec_lse[static_cast<long long>(rec) * G + n] = l_[e] > 0.f ? mm[e] + __log2f(l_[e]) : -INFINITY;
+    }
+  };
+
+  while (ci < ntiles) {
+    // ---------------- producer: fill free stages with chunks. A chunk is up
+    // to kChunk tiles of one segment; a new segment needs a free query buffer
+    // (the consumer must have begun the one before it).
+    while (!p_done && !((stage_busy >> p_stage) & 1u)) {
+      const int seg = segment_of(pw, a);
+      if (seg != p_seg) {
+        if (p_seg >= 0 && c_seg < p_seg) break;
         p_qslot ^= 1;
-        if (p_qslot) ++q_iss1; else ++q_iss0;
+        q_pending |= 1u << p_qslot;
         if (lane == 0) {
           const uint32_t bar = bars + 8 * (kStages + p_qslot);
           const uint8_t* src = static_cast<const uint8_t*>(a.q) +
-                               (static_cast<long long>(pw.b) * a.n_q + static_cast<long long>(pw.h) * G) * kD * 2;
+                               (static_cast<long long>(pw.b) * a.n_q + pw.h * G) * (kD * 2);
           fence_proxy_async();
-          mbar_expect(bar, G * kD * 2);
-          bulk_g2s_plain(qbuf + p_qslot * kQBufBytes, src, G * kD * 2, bar);
+          mbar_expect(bar, a.qbuf_bytes);
+          bulk_g2s_plain(qbuf + p_qslot * a.qbuf_bytes, src, a.qbuf_bytes, bar);
         }
         p_seg = seg;
       }
-      const int stage = static_cast<int>(pi % kStages);
-      const int blk_i = (pw.t << 4) >> a.log2_bs;   // block index within the sequence
-      if (pw.b != bid_b || blk_i - bid_base >= 32 || blk_i < bid_base) {
-        bid_b = pw.b;
-        bid_base = blk_i;
-        const int j = bid_base + lane;
-        bid_reg = (j * a.block_size < pw.len) ? __ldg(a.block_table + static_cast<long long>(pw.b) * a.bt_stride + j) : -1;
-      }
-      const int blk = __shfl_sync(0xffffffffu, bid_reg, blk_i - bid_base);
-      const bool ok = blk >= 0 && blk < a.num_blocks;
-      if (lane == 0) {
-        const uint32_t bar = bars + 8 * stage;
-        if (ok) {
-          const uint8_t* src = a.cache + ((static_cast<long long>(blk) * a.n_kv + pw.h) * a.tiles_per_block +
-                                          (pw.t & (a.tiles_per_block - 1))) *
-                                             static_cast<long long>(a.tile_bytes);
-          fence_proxy_async();
-          mbar_expect(bar, a.tile_bytes);
-          bulk_g2s(ring + stage * a.tile_stride, src, a.tile_bytes, bar, policy);
-        } else {
-          mbar_expect(bar, 0);   // completes the phase with no data
+      const uint32_t bar = bars + 8 * p_stage;
+      if (lane == 0) fence_proxy_async();
+      uint32_t okm = 0;
+      int n = 0;
+      for (;;) {
+        const int blk_i = (pw.t << 4) >> a.log2_bs;   // block index within the sequence
+        if (pw.b != bid_b || blk_i - bid_base >= 32 || blk_i < bid_base) {
+          bid_b = pw.b;
+          bid_base = blk_i;
+          const int j = bid_base + lane;
+          bid_reg = (j * a.block_size < pw.len) ? __ldg(a.block_table + static_cast<long long>(pw.b) * a.bt_stride + j) : -1;
         }
+        const int blk = __shfl_sync(0xffffffffu, bid_reg, blk_i - bid_base);
+        if (blk >= 0 && blk < a.num_blocks) {
+          okm |= 1u << n;
+          if (lane == 0) {
+            const uint8_t* src = a.cache + ((static_cast<long long>(blk) * a.n_kv + pw.h) * a.tiles_per_block +
+                                            (pw.t & (a.tiles_per_block - 1))) *
+                                               static_cast<long long>(a.tile_bytes);
+            mbar_expect_tx(bar, a.tile_bytes);
+            bulk_g2s(ring + p_stage * a.stage_bytes + n * a.tile_bytes, src, a.tile_bytes, bar, policy);
+          }
+        }
+        ++n;
+        ++pi;
+        if (pi >= ntiles || !walk_next(pw, a, lane)) { p_done = true; break; }
+        if (n == kChunk || segment_of(pw, a) != seg) break;
       }
-      tile_ok_bits = ok ? (tile_ok_bits | (1u << stage)) : (tile_ok_bits & ~(1u << stage));
-      ++pi;
-      if (pi >= r1 || !walk_next(pw, a, lane)) p_done = true;
+      if (lane == 0) mbar_arrive(bar);
+      ok_bits = (ok_bits & ~(((1u << kChunk) - 1) << (kChunk * p_stage))) | (okm << (kChunk * p_stage));
+      stage_busy |= 1u << p_stage;
+      p_stage = p_stage + 1 == kStages ? 0 : p_stage + 1;
     }
 
     // ---------------- consumer
-    const long long seg = segment_of(cw, a);
+    const int seg = segment_of(cw, a);
     if (seg != c_seg) {
-      if (c_seg >= 0) {
-        // ---- finalize the previous segment: combine hi/lo columns, add
-        // sum p * zero, normalise, write its record
-        float l = lsum, z = zsum;
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        z += __shfl_xor_sync(0xffffffffu, z, 1);
-        z += __shfl_xor_sync(0xffffffffu, z, 2);
-        const long long rec = c_seg + wid;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int n = 2 * c + e;            // this lane's column = query head n
-          const int pc = n + G;               // its lo column when G <= 4
-          const int src = 4 * g + ((pc >> 1) & 3);
-          const int hh = n < G ? n : 0;
-          const float lh = __shfl_sync(0xffffffffu, l, 4 * hh);
-          const float zh = __shfl_sync(0xffffffffu, z, 4 * hh);
-          const float mh = __shfl_sync(0xffffffffu, mrow, 4 * hh);
-          const float inv = lh > 0.f ? 1.f / lh : 0.f;
-          float* dst = a.rec_o + (rec * G + hh) * kD + 16 * g;
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            float v0 = o[mt][e], v1 = o[mt][2 + e];
-            if (!GBIG) {
-              const float p0 = __shfl_sync(0xffffffffu, o[mt][0], src);
-              const float p1 = __shfl_sync(0xffffffffu, o[mt][1], src);
-              const float p2 = __shfl_sync(0xffffffffu, o[mt][2], src);
-              const float p3 = __shfl_sync(0xffffffffu, o[mt][3], src);
-              v0 += (pc & 1) ? p1 : p0;
-              v1 += (pc & 1) ? p3 : p2;
-            }
-            if (n < G) *reinterpret_cast<float2*>(dst + 2 * mt) = make_float2((v0 + zh) * inv, (v1 + zh) * inv);
-          }
-          if (n < G && g == 0) a.rec_lse[rec * G + n] = lh > 0.f ? mh + __log2f(lh) : -INFINITY;
-        }
-      }
-      // ---- begin the new segment: wait for its query rows, rotate, split
+      if (c_seg >= 0) finalize(c_seg);
+      // ---- begin the segment: its query rows, rotated, scaled, split hi/lo
       c_qslot ^= 1;
-      const unsigned uses = c_qslot ? q_uses1 : q_uses0;
-      if (!mbar_wait(bars + 8 * (kStages + c_qslot), uses & 1)) { aborted = true; break; }
-      if (c_qslot) ++q_uses1; else ++q_uses0;
-      uint32_t hp[8][4];   // [head][hi01, lo01, hi23, lo23] of this lane's 4 coordinates
+      if (!mbar_wait(bars + 8 * (kStages + c_qslot), (q_phase >> c_qslot) & 1u)) { aborted = true; break; }
+      q_phase ^= 1u << c_qslot;
+      q_pending &= ~(1u << c_qslot);
+#pragma unroll
+      for (int i = 0; i < (GBIG ? 32 : 16); ++i) qb[i] = 0u;
 #pragma unroll
       for (int gg = 0; gg < 8; ++gg) {
-        hp[gg][0] = hp[gg][1] = hp[gg][2] = hp[gg][3] = 0u;
         if (gg < G) {
           float x[4];
-          u2_to_f4<TQ>(lds64(qbuf + c_qslot * kQBufBytes + gg * kD * 2 + 8 * lane), x);
+          u2_to_f4<TQ>(lds64(qbuf + c_qslot * a.qbuf_bytes + gg * kD * 2 + 8 * lane), x);
           float sc = a.qscale;
           if constexpr (KMODE != kFp8) {
             fwht128(x, lane);
             sc *= 0.088388347648318440f;   // 1 / sqrt(128)
           }
-          split_half2(x[0] * sc, x[1] * sc, hp[gg][0], hp[gg][1]);
-          split_half2(x[2] * sc, x[3] * sc, hp[gg][2], hp[gg][3]);
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) qa[i] = 0u;
-#pragma unroll
-      for (int gg = 0; gg < 8; ++gg) {
-        if (gg < G) {
+          uint32_t hp[4];   // hi01, lo01, hi23, lo23 of coordinates 4 lane .. +3
+          split_half2(x[0] * sc, x[1] * sc, hp[0], hp[1]);
+          split_half2(x[2] * sc, x[3] * sc, hp[2], hp[3]);
+          // B column g takes head gg's hi part (g == gg) or lo part (g == gg + G)
+          const bool take_hi = g == gg, take_lo = GBIG ? (g == gg) : (g == gg + G);
           if constexpr (KMODE == kFp8) {
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {   // coordinates 32 c + 4 s .. +3 live in lane 8 c + s
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint32_t v = __shfl_sync(0xffffffffu, hp[gg][k], 8 * c + s);
-                if (g == gg) qa[4 * s + k] = v;
+            for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3 live in lane 8c + s
+              const uint32_t h01 = __shfl_sync(0xffffffffu, hp[0], 8 * c + s);
+              const uint32_t l01 = __shfl_sync(0xffffffffu, hp[1], 8 * c + s);
+              const uint32_t h23 = __shfl_sync(0xffffffffu, hp[2], 8 * c + s);
+              const uint32_t l23 = __shfl_sync(0xffffffffu, hp[3], 8 * c + s);
+              if (GBIG) {
+                if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; qb[16 + 2 * s] = l01; qb[16 + 2 * s + 1] = l23; }
+              } else {
+                if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; }
+                if (take_lo) { qb[2 * s] = l01; qb[2 * s + 1] = l23; }
               }
             }
           } else {
 #pragma unroll
-            for (int s = 0; s < 16; ++s) {  // coordinates 32 c + 2 s, +1 live in lane 8 c + s / 2
-              const int sl = 8 * c + (s >> 1);
-              const uint32_t vh = __shfl_sync(0xffffffffu, (s & 1) ? hp[gg][2] : hp[gg][0], sl);
-              const uint32_t vl = __shfl_sync(0xffffffffu, (s & 1) ? hp[gg][3] : hp[gg][1], sl);
-              if (g == gg) { qa[2 * s] = vh; qa[2 * s + 1] = vl; }
+            for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3 live in lane 8c + s
+              const uint32_t h01 = __shfl_sync(0xffffffffu, hp[0], 8 * c + s);
+              const uint32_t l01 = __shfl_sync(0xffffffffu, hp[1], 8 * c + s);
+              const uint32_t h23 = __shfl_sync(0xffffffffu, hp[2], 8 * c + s);
+              const uint32_t l23 = __shfl_sync(0xffffffffu, hp[3], 8 * c + s);
+              if (GBIG) {
+                if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; qb[16 + 2 * s] = l01; qb[16 + 2 * s + 1] = l23; }
+              } else {
+                if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; }
+                if (take_lo) { qb[2 * s] = l01; qb[2 * s + 1] = l23; }
+              }
             }
           }
         }
       }
-      __syncwarp();   // q buffer fully read before the producer may reuse it
+      __syncwarp();   // query buffer fully read before the producer may reuse it
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-      mrow = mc0 = mc1 = -INFINITY;
-      lsum = zsum = 0.f;
+      m0 = m1 = -INFINITY;
+      l0 = l1 = z0 = z1 = 0.f;
       c_seg = seg;
     }
 
-    const int stage = static_cast<int>(ci % kStages);
-    if (!mbar_wait(bars + 8 * stage, static_cast<uint32_t>((ci / kStages) & 1))) { aborted = true; break; }
-    const bool ok = (tile_ok_bits >> stage) & 1u;
-    if (!ok) {
-      if (lane == 0) flag(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
-      __syncwarp();
-    } else {
-      const uint32_t st = ring + stage * a.tile_stride;
-      const int nvalid = min(kTileTokens, cw.len - (cw.t << 4));
-      // ---- this lane's slice of the tile
-      uint4 kq[KMODE == kFp8 ? 4 : 2];
-      if constexpr (KMODE == kMse4) {
-        kq[0] = lds128(st + a.k_off + g * 64 + 16 * c);
-        kq[1] = lds128(st + a.k_off + (g + 8) * 64 + 16 * c);
-      } else if constexpr (KMODE == kMse3) {
-        const uint32_t ra = st + a.k_off + g * 48 + 12 * c, rb = st + a.k_off + (g + 8) * 48 + 12 * c;
-        kq[0] = make_uint4(lds32(ra), lds32(ra + 4), lds32(ra + 8), 0u);
-        kq[1] = make_uint4(lds32(rb), lds32(rb + 4), lds32(rb + 8), 0u);
-      } else {
-        kq[0] = lds128(st + a.k_off + g * 128 + 32 * c);
-        kq[1] = lds128(st + a.k_off + g * 128 + 32 * c + 16);
-        kq[2] = lds128(st + a.k_off + (g + 8) * 128 + 32 * c);
-        kq[3] = lds128(st + a.k_off + (g + 8) * 128 + 32 * c + 16);
-      }
-      const uint4 va = lds128(st + a.v_off + c * 128 + 16 * g);
-      const uint4 vb = lds128(st + a.v_off + (c + 4) * 128 + 16 * g);
-      float2 n01 = make_float2(1.f, 1.f), n89 = make_float2(1.f, 1.f);
-      if constexpr (KMODE != kFp8) {
-        n01 = half2_bits_to_float2(lds32(st + a.knorm_off + 4 * c));
-        n89 = half2_bits_to_float2(lds32(st + a.knorm_off + 16 + 4 * c));
-      }
-      const float2 s01 = half2_bits_to_float2(lds32(st + a.vscale_off + 4 * c));
-      const float2 s89 = half2_bits_to_float2(lds32(st + a.vscale_off + 16 + 4 * c));
-      const float2 z01 = half2_bits_to_float2(lds32(st + a.vzero_off + 4 * c));
-      const float2 z89 = half2_bits_to_float2(lds32(st + a.vzero_off + 16 + 4 * c));
-      __syncwarp();   // every lane has read the stage: the producer may refill it
+    // chunk of this stage: n tiles from cw (same rule as the producer)
+    int n = 1;
+    {
+      Walk t = cw;
+      while (n < kChunk && ci + n < ntiles && walk_next(t, a, lane) && segment_of(t, a) == seg) ++n;
+    }
+    if (!mbar_wait(bars + 8 * c_stage, (c_phase >> c_stage) & 1u)) { aborted = true; break; }
+    c_phase ^= 1u << c_stage;
+    const uint32_t okm = (ok_bits >> (kChunk * c_stage)) & ((1u << kChunk) - 1);
+    if (okm != (1u << n) - 1 && lane == 0) flag(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
+    const uint32_t st = ring + c_stage * a.stage_bytes;
+    const int tok0 = cw.t << 4;   // first position of the chunk in its sequence
 
-      // ---- scores: tokens 2c, 2c+1 (n-tile 0) and 2c+8, 2c+9 (n-tile 1)
-      float s0[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      float s1[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      qk_tile<KMODE>(s0, qa, &kq[0], lut_lane);
-      qk_tile<KMODE>(s1, qa, &kq[KMODE == kFp8 ? 2 : 1], lut_lane);
-      float sc[4];
-      sc[0] = ((s0[0][0] + s0[1][0]) + (s0[0][2] + s0[1][2])) * n01.x;
-      sc[1] = ((s0[0][1] + s0[1][1]) + (s0[0][3] + s0[1][3])) * n01.y;
-      sc[2] = ((s1[0][0] + s1[1][0]) + (s1[0][2] + s1[1][2])) * n89.x;
-      sc[3] = ((s1[0][1] + s1[1][1]) + (s1[0][3] + s1[1][3])) * n89.y;
-      float vs[4] = {s01.x, s01.y, s89.x, s89.y};
-      float vz[4] = {z01.x, z01.y, z89.x, z89.y};
-      if (nvalid < kTileTokens) {   // ragged last tile of a sequence
-        const int tk[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+    // ---- S[i] = K_i . Q^T for the chunk's tiles (missing tiles compute on
+    // stale bytes and are masked below)
+    float S[kChunk][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (tk[e] >= nvalid) { sc[e] = -INFINITY; vs[e] = 0.f; vz[e] = 0.f; }
-      }
-      float cm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-      cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
-      cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
-      const float cm0 = __shfl_sync(0xffffffffu, cm, 4 * rc0);
-      const float cm1 = __shfl_sync(0xffffffffu, cm, 4 * rc1);
-      const float ar = lazy_update(mrow, cm);
-      const float a0 = lazy_update(mc0, cm0);
-      const float a1 = lazy_update(mc1, cm1);
-      if (ar != 1.f) { lsum *= ar; zsum *= ar; }
-      if (a0 != 1.f) {
+    for (int i = 0; i < kChunk; ++i) S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0.f;
+    if constexpr (KMODE == kFp8) {
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) { o[mt][0] *= a0; o[mt][2] *= a0; }
-      }
-      if (a1 != 1.f) {
+      for (int i = 0; i < kChunk; ++i) {
+        const uint32_t kt = st + i * a.tile_bytes + a.k_off;
+        const uint4 kg0 = lds128(kt + g * 128 + 32 * c), kg1 = lds128(kt + g * 128 + 32 * c + 16);
+        const uint4 kh0 = lds128(kt + (g + 8) * 128 + 32 * c), kh1 = lds128(kt + (g + 8) * 128 + 32 * c + 16);
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) { o[mt][1] *= a1; o[mt][3] *= a1; }
-      }
-      float ps[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float pe = ex2(sc[e] - mrow);   // exp2(-inf) = 0 for masked tokens
-        lsum += pe;
-        ps[e] = pe * vs[e];
-        zsum = fmaf(pe, vz[e], zsum);
-      }
-      uint32_t hi01, lo01, hi23, lo23;
-      split_half2(ps[0], ps[1], hi01, lo01);
-      split_half2(ps[2], ps[3], hi23, lo23);
-      const bool real_row = g < G;
-      if (GBIG) {
-        const uint32_t b0h = real_row ? hi01 : 0u, b1h = real_row ? hi23 : 0u;
-        const uint32_t b0l = real_row ? lo01 : 0u, b1l = real_row ? lo23 : 0u;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const uint32_t wa = word_of(va, mt >> 1), wb = word_of(vb, mt >> 1);
-          const int j0 = 2 * (mt & 1);
-          const uint32_t v0 = vpair(wa, j0), v1 = vpair(wa, j0 + 1);
-          const uint32_t v2 = vpair(wb, j0), v3 = vpair(wb, j0 + 1);
-          mma16816(o[mt], v0, v1, v2, v3, b0h, b1h);
-          mma16816(o[mt], v0, v1, v2, v3, b0l, b1l);
+        for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3
+          const uint32_t wg = word_of(s < 4 ? kg0 : kg1, s & 3), wh = word_of(s < 4 ? kh0 : kh1, s & 3);
+          const __half2_raw g01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wg & 0xFFFFu), __NV_E4M3);
+          const __half2_raw g23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wg >> 16), __NV_E4M3);
+          const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh & 0xFFFFu), __NV_E4M3);
+          const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh >> 16), __NV_E4M3);
+          const uint32_t a0 = static_cast<uint32_t>(g01.x) | (static_cast<uint32_t>(g01.y) << 16);
+          const uint32_t a1 = static_cast<uint32_t>(h01.x) | (static_cast<uint32_t>(h01.y) << 16);
+          const uint32_t a2 = static_cast<uint32_t>(g23.x) | (static_cast<uint32_t>(g23.y) << 16);
+          const uint32_t a3 = static_cast<uint32_t>(h23.x) | (static_cast<uint32_t>(h23.y) << 16);
+          mma16816(S[i], a0, a1, a2, a3, qb[2 * s], qb[2 * s + 1]);
+          if (GBIG) mma16816(S[i], a0, a1, a2, a3, qb[16 + 2 * s], qb[16 + 2 * s + 1]);
         }
-      } else {
-        const int src = (lane - 4 * G) & 31;
-        const uint32_t t01 = __shfl_sync(0xffffffffu, lo01, src);
-        const uint32_t t23 = __shfl_sync(0xffffffffu, lo23, src);
-        const uint32_t b0 = real_row ? hi01 : (g < 2 * G ? t01 : 0u);
-        const uint32_t b1 = real_row ? hi23 : (g < 2 * G ? t23 : 0u);
+      }
+    } else {
+      uint4 kg[kChunk], kh[kChunk];   // this lane's key slice of tokens g and g+8
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const uint32_t wa = word_of(va, mt >> 1), wb = word_of(vb, mt >> 1);
-          const int j0 = 2 * (mt & 1);
-          mma16816(o[mt], vpair(wa, j0), vpair(wa, j0 + 1), vpair(wb, j0), vpair(wb, j0 + 1), b0, b1);
+      for (int i = 0; i < kChunk; ++i) {
+        const uint32_t kt = st + i * a.tile_bytes + a.k_off;
+        if constexpr (KMODE == kMse4) {
+          kg[i] = lds128(kt + g * 64 + 16 * c);
+          kh[i] = lds128(kt + (g + 8) * 64 + 16 * c);
+        } else {
+          const uint32_t ra = kt + g * 48 + 12 * c, rb = kt + (g + 8) * 48 + 12 * c;
+          kg[i] = make_uint4(lds32(ra), lds32(ra + 4), lds32(ra + 8), 0u);
+          kh[i] = make_uint4(lds32(rb), lds32(rb + 4), lds32(rb + 8), 0u);
+        }
+      }
+      // M rows: 8 tokens x {centroid hi part, centroid lo part}; k-step s holds
+      // this lane's coordinates 32c + 4s .. +3 (two key bytes = two LUT entries,
+      // each entry = the (hi, lo) operand pair of one row pair)
+      float Sl[kChunk][2][4];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) Sl[i][u][0] = Sl[i][u][1] = Sl[i][u][2] = Sl[i][u][3] = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2) {
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+          const uint2 g0 = lds64(lut_addr<KMODE>(kg[i], 2 * s2, lut_lane));
+          const uint2 g1 = lds64(lut_addr<KMODE>(kg[i], 2 * s2 + 1, lut_lane));
+          const uint2 h0 = lds64(lut_addr<KMODE>(kh[i], 2 * s2, lut_lane));
+          const uint2 h1 = lds64(lut_addr<KMODE>(kh[i], 2 * s2 + 1, lut_lane));
+          mma16816(Sl[i][0], g0.x, g0.y, g1.x, g1.y, qb[2 * s2], qb[2 * s2 + 1]);
+          mma16816(Sl[i][1], h0.x, h0.y, h1.x, h1.y, qb[2 * s2], qb[2 * s2 + 1]);
+          if (GBIG) {
+            mma16816(Sl[i][0], g0.x, g0.y, g1.x, g1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
+            mma16816(Sl[i][1], h0.x, h0.y, h1.x, h1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
+          }
+        }
+      }
+      // rows g (hi part) + g + 8 (lo part) of each token: same lane
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        S[i][0] = Sl[i][0][0] + Sl[i][0][2];
+        S[i][1] = Sl[i][0][1] + Sl[i][0][3];
+        S[i][2] = Sl[i][1][0] + Sl[i][1][2];
+        S[i][3] = Sl[i][1][1] + Sl[i][1][3];
+      }
+    }
+
+    // ---- scores: combine q_lo columns, norms, masks; per-head chunk max
+    // S[i]: [0] tok g col 2c, [1] tok g col 2c+1, [2] tok g+8 col 2c, [3] tok g+8 col 2c+1
+    float sv[kChunk][2], sz[kChunk][2];   // value scale / zero of tokens g, g+8
+    float cm0 = -INFINITY, cm1 = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const uint32_t tb = st + i * a.tile_bytes;
+      float* v = S[i];
+      if (!GBIG) {   // add the q_lo column of each head (column + G)
+        const int srcA = 4 * g + (((2 * c + G) >> 1) & 3), srcB = 4 * g + (((2 * c + 1 + G) >> 1) & 3);
+        const bool odd = G & 1;
+        const float t0 = __shfl_sync(0xffffffffu, odd ? v[1] : v[0], srcA);
+        const float t2 = __shfl_sync(0xffffffffu, odd ? v[3] : v[2], srcA);
+        const float t1 = __shfl_sync(0xffffffffu, odd ? v[0] : v[1], srcB);
+        const float t3 = __shfl_sync(0xffffffffu, odd ? v[2] : v[3], srcB);
+        v[0] += t0; v[1] += t1; v[2] += t2; v[3] += t3;
+      }
+      if constexpr (KMODE != kFp8) {
+        const float ng = lds_h2f(tb + a.knorm_off + 2 * g), nh = lds_h2f(tb + a.knorm_off + 2 * g + 16);
+        v[0] *= ng; v[1] *= ng; v[2] *= nh; v[3] *= nh;
+      }
+      sv[i][0] = lds_h2f(tb + a.vscale_off + 2 * g);
+      sv[i][1] = lds_h2f(tb + a.vscale_off + 2 * g + 16);
+      sz[i][0] = lds_h2f(tb + a.vzero_off + 2 * g);
+      sz[i][1] = lds_h2f(tb + a.vzero_off + 2 * g + 16);
+      const int nvalid = ((okm >> i) & 1u) ? min(kTileTokens, cw.len - tok0 - 16 * i) : 0;
+      if (nvalid < kTileTokens) {   // missing or ragged tile
+        if (g >= nvalid) { v[0] = v[1] = -INFINITY; sv[i][0] = 0.f; sz[i][0] = 0.f; }
+        if (g + 8 >= nvalid) { v[2] = v[3] = -INFINITY; sv[i][1] = 0.f; sz[i][1] = 0.f; }
+      }
+      cm0 = fmaxf(cm0, fmaxf(v[0], v[2]));
+      cm1 = fmaxf(cm1, fmaxf(v[1], v[3]));
+    }
+#pragma unroll
+    for (int o_ = 4; o_ < 32; o_ <<= 1) {
+      cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, o_));
+      cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, o_));
+    }
+    const bool need = (2 * c < G && cm0 > m0 + kTau) || (2 * c + 1 < G && cm1 > m1 + kTau);
+    if (__any_sync(0xffffffffu, need)) {   // rare: move the running max, rescale
+      float al0 = 1.f, al1 = 1.f;
+      if (cm0 > m0 + kTau) { al0 = ex2(m0 - cm0); m0 = cm0; }
+      if (cm1 > m1 + kTau) { al1 = ex2(m1 - cm1); m1 = cm1; }
+      l0 *= al0; z0 *= al0; l1 *= al1; z1 *= al1;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {   // O^T column 2c + e belongs to head hn
+        const int nn = 2 * c + e;
+        const int hn = GBIG ? nn : (nn < G ? nn : (nn < 2 * G ? nn - G : 0));
+        const float x0 = __shfl_sync(0xffffffffu, al0, 4 * g + (hn >> 1));
+        const float x1 = __shfl_sync(0xffffffffu, al1, 4 * g + (hn >> 1));
+        const float al = (hn & 1) ? x1 : x0;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) { o[mt][e] *= al; o[mt][2 + e] *= al; }
+      }
+    }
+
+    // ---- per tile: probabilities, P^T operands (movmatrix), O^T += V^T . P^T
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const float* v = S[i];
+      // fmaxf also maps the NaN of (-inf) - (-inf) (a fully masked chunk before
+      // any valid position) to an argument whose exp2 is 0
+      const float p0 = ex2(fmaxf(v[0] - m0, -200.f)), p1 = ex2(fmaxf(v[1] - m1, -200.f));
+      const float p2 = ex2(fmaxf(v[2] - m0, -200.f)), p3 = ex2(fmaxf(v[3] - m1, -200.f));
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      z0 = fmaf(p0, sz[i][0], fmaf(p2, sz[i][1], z0));
+      z1 = fmaf(p1, sz[i][0], fmaf(p3, sz[i][1], z1));
+      uint32_t hg, lg, hh, lh;   // hi/lo half2 of (col 2c, col 2c+1) for tokens g and g+8
+      split_half2(p0 * sv[i][0], p1 * sv[i][0], hg, lg);
+      split_half2(p2 * sv[i][1], p3 * sv[i][1], hh, lh);
+      uint32_t mg, mh, mgl = 0u, mhl = 0u;   // P matrices [token][column] in mma layout
+      if (GBIG) {
+        const uint32_t keep = (2 * c + 1 < G) ? 0xFFFFFFFFu : ((2 * c < G) ? 0x0000FFFFu : 0u);
+        mg = hg & keep; mh = hh & keep; mgl = lg & keep; mhl = lh & keep;
+      } else {
+        // column n < G: hi of head n (own); G <= n < 2G: lo of head n - G
+        uint32_t sel_g = 0u, sel_h = 0u;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int nn = 2 * c + e;
+          const int hn = nn - G;
+          const int src = 4 * g + ((hn >> 1) & 3);
+          const uint32_t wg = __shfl_sync(0xffffffffu, lg, src);
+          const uint32_t wh = __shfl_sync(0xffffffffu, lh, src);
+          uint32_t xg, xh;
+          if (nn < G) {
+            xg = e ? (hg >> 16) : (hg & 0xFFFFu);
+            xh = e ? (hh >> 16) : (hh & 0xFFFFu);
+          } else if (nn < 2 * G) {
+            xg = (hn & 1) ? (wg >> 16) : (wg & 0xFFFFu);
+            xh = (hn & 1) ? (wh >> 16) : (wh & 0xFFFFu);
+          } else {
+            xg = xh = 0u;
+          }
+          sel_g |= xg << (16 * e);
+          sel_h |= xh << (16 * e);
+        }
+        mg = sel_g;
+        mh = sel_h;
+      }
+      const uint32_t b0 = movmatrix_trans(mg), b1 = movmatrix_trans(mh);
+      const uint32_t tb = st + i * a.tile_bytes + a.v_off + 16 * (g ^ (2 * c));
+      const uint4 va = lds128(tb + 128 * c);         // tokens 2c, 2c+1
+      const uint4 vb = lds128(tb + 128 * (c + 4));   // tokens 2c+8, 2c+9
+      uint32_t b0l = 0u, b1l = 0u;
+      if (GBIG) { b0l = movmatrix_trans(mgl); b1l = movmatrix_trans(mhl); }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t wa = word_of(va, k), wb = word_of(vb, k);
+        const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+        mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0, b1);
+        mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0, b1);
+        if (GBIG) {
+          mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0l, b1l);
+          mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0l,
+                   b1l);
         }
       }
     }
-    ++ci;
-    if (ci < r1) walk_next(cw, a, lane);
+    __syncwarp();   // every lane has read the stage: the producer may refill it
+    stage_busy &= ~(1u << c_stage);
+    c_stage = c_stage + 1 == kStages ? 0 : c_stage + 1;
+    ci += n;
+    for (int i = 0; i < n && ci < ntiles; ++i) walk_next(cw, a, lane);
   }
 
   if (!aborted) {
-    // ---- finalize the last segment
-    float l = lsum, z = zsum;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    z += __shfl_xor_sync(0xffffffffu, z, 1);
-    z += __shfl_xor_sync(0xffffffffu, z, 2);
-    const long long rec = c_seg + wid;
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int n = 2 * c + e;
-      const int pc = n + G;
-      const int src = 4 * g + ((pc >> 1) & 3);
-      const int hh = n < G ? n : 0;
-      const float lh = __shfl_sync(0xffffffffu, l, 4 * hh);
-      const float zh = __shfl_sync(0xffffffffu, z, 4 * hh);
-      const float mh = __shfl_sync(0xffffffffu, mrow, 4 * hh);
-      const float inv = lh > 0.f ? 1.f / lh : 0.f;
-      float* dst = a.rec_o + (rec * G + hh) * kD + 16 * g;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        float v0 = o[mt][e], v1 = o[mt][2 + e];
-        if (!GBIG) {
-          const float p0 = __shfl_sync(0xffffffffu, o[mt][0], src);
-          const float p1 = __shfl_sync(0xffffffffu, o[mt][1], src);
-          const float p2 = __shfl_sync(0xffffffffu, o[mt][2], src);
-          const float p3 = __shfl_sync(0xffffffffu, o[mt][3], src);
-          v0 += (pc & 1) ? p1 : p0;
-          v1 += (pc & 1) ? p3 : p2;
-        }
-        if (n < G) *reinterpret_cast<float2*>(dst + 2 * mt) = make_float2((v0 + zh) * inv, (v1 + zh) * inv);
-      }
-      if (n < G && g == 0) a.rec_lse[rec * G + n] = lh > 0.f ? mh + __log2f(lh) : -INFINITY;
-    }
+    finalize(c_seg);
   } else {
     // a wait expired: flag it and drain this warp's own copies (bounded) so no
     // bulk copy still targets shared memory when the warp stops
     if (lane == 0) flag(a.status, TQ_DEV_TIMEOUT);
-    for (long long i = ci; i < pi; ++i)
-      mbar_wait(bars + 8 * static_cast<int>(i % kStages), static_cast<uint32_t>((i / kStages) & 1));
-    if (q_iss0 > q_uses0) mbar_wait(bars + 8 * kStages, q_uses0 & 1);
-    if (q_iss1 > q_uses1) mbar_wait(bars + 8 * (kStages + 1), q_uses1 & 1);
+    for (int s = 0; s < kStages; ++s)
+      if ((stage_busy >> s) & 1u) mbar_wait(bars + 8 * s, (c_phase >> s) & 1u);
+    for (int qs = 0; qs < 2; ++qs)
+      if ((q_pending >> qs) & 1u) mbar_wait(bars + 8 * (kStages + qs), (q_phase >> qs) & 1u);
   }
 }
 
@@ -834,7 +902,7 @@ __global__ void __launch_bounds__(kD) reduce_kernel(const ReduceArgs a) {
 
 struct Plan {
   tq_layout L;
-  int part_tiles, num_parts, cap, sms, num_warps;
+  int part_tiles, num_parts, cap, sms;
   long long num_records;
   size_t need;
 };
@@ -846,8 +914,8 @@ int device_sms() {
   return sms;
 }
 
-// Host-side checks and sizes shared by both stages (no CUDA call before the
-// argument checks pass; the SM count is queried last).
+// Host-side checks and sizes shared by both stages (no CUDA call unless
+// query_device; the workspace size never depends on the device).
 tq_status make_plan(const tq_config* cfg, int batch, int max_seq_len, int bt_stride, bool query_device,
                     Plan* P) {
   tq_status st = make_layout(cfg, &P->L);
@@ -863,33 +931,69 @@ tq_status make_plan(const tq_config* cfg, int batch, int max_seq_len, int bt_str
   P->cap = bt_stride * cfg->block_size;
   P->sms = query_device ? device_sms() : 0;
   if (P->sms > kMaxCtas) P->sms = kMaxCtas;
-  P->num_warps = (P->sms > 0 ? P->sms : 1) * kWarps;
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
   P->num_records = static_cast<long long>(batch) * cfg->num_kv_heads * P->num_parts +
-                   static_cast<long long>(kMaxCtas) * kWarps;
+                   static_cast<long long>(kMaxCtas) * kRecordWarps;
+  if (P->num_records > (1ll << 30)) return TQ_ERR_UNSUPPORTED;
   const long long floats = P->num_records * G * (kD + 1);
   P->need = static_cast<size_t>(((floats * 4 + 15) / 16) * 16);
   return TQ_OK;
 }
 
-int warp_buffer_bytes(int tile_bytes) {
-  const int stride = (tile_bytes + 127) & ~127;
-  return kStages * stride + 2 * kQBufBytes + 8 * (kStages + 2);
+struct LaunchShape {
+  int warps;        // per CTA
+  int warp_bytes;
+  int stage_bytes;
+  int dyn_bytes;
+};
+
+// Warps whose buffers fit around a LUT aligned to its size, for a dynamic
+// shared-memory window starting at `start` (the plan the kernel computes).
+int warps_that_fit(uint32_t start, uint32_t dyn, uint32_t lut, uint32_t wb) {
+  const uint32_t lut_at = lut ? ((start + lut - 1) & ~(lut - 1)) : start + dyn;
+  if (lut && lut_at + lut > start + dyn) return 0;
+  int n = 0;
+  uint32_t p = start;
+  for (;;) {
+    if (lut && p < lut_at + lut && p + wb > lut_at) p = lut_at + lut;
+    if (p + wb > start + dyn) return n;
+    p += wb;
+    ++n;
+  }
+}
+
+template <int KMODE>
+bool launch_shape(int tile_bytes, int group, LaunchShape* s) {
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
+  s->stage_bytes = kChunk * tile_bytes;
+  s->warp_bytes = kStages * s->stage_bytes + 2 * group * kD * 2 + 8 * (kStages + 2);
+  s->warp_bytes = (s->warp_bytes + 15) & ~15;
+  const uint32_t lut = lut_bytes<KMODE>();
+  // the window may start at 0 or after a small reserved area; take the worse
+  int warps = warps_that_fit(0, optin, lut, s->warp_bytes);
+  const int w2 = warps_that_fit(1024, optin, lut, s->warp_bytes);
+  if (w2 < warps) warps = w2;
+  if (warps > kMaxWarps) warps = kMaxWarps;
+  if (warps < 1) return false;
+  s->warps = warps;
+  s->dyn_bytes = optin;
+  return true;
 }
 
 template <int KMODE, int GBIG, typename TQ>
 cudaError_t launch_split_typed(DecodeArgs a, cudaStream_t s, int sms) {
-  int dev = 0, optin = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  a.tile_stride = (a.tile_bytes + 127) & ~127;
-  a.warp_bytes = warp_buffer_bytes(a.tile_bytes);
-  const int want = kWarps * a.warp_bytes + static_cast<int>(2 * lut_bytes<KMODE>());
-  a.dyn_bytes = want < optin ? want : optin;
+  LaunchShape sh;
+  if (!launch_shape<KMODE>(a.tile_bytes, a.group, &sh)) return cudaErrorInvalidConfiguration;
+  a.stage_bytes = sh.stage_bytes;
+  a.warp_bytes = sh.warp_bytes;
+  a.dyn_bytes = sh.dyn_bytes;
+  a.qbuf_bytes = a.group * kD * 2;
   auto k = split_kernel<KMODE, GBIG, TQ>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, a.dyn_bytes);
   if (err != cudaSuccess) return err;
-  k<<<static_cast<unsigned>(sms), kWarps * 32, static_cast<size_t>(a.dyn_bytes), s>>>(a);
+  k<<<static_cast<unsigned>(sms), sh.warps * 32, static_cast<size_t>(a.dyn_bytes), s>>>(a);
   return cudaGetLastError();
 }
 
@@ -900,6 +1004,15 @@ cudaError_t launch_split(const DecodeArgs& a, int q_dtype, cudaStream_t s, int s
                        : launch_split_typed<KMODE, 0, __nv_bfloat16>(a, s, sms);
   return a.group > 4 ? launch_split_typed<KMODE, 1, __half>(a, s, sms)
                      : launch_split_typed<KMODE, 0, __half>(a, s, sms);
+}
+
+int split_warps_per_cta(const tq_layout& L, int group) {
+  LaunchShape sh;
+  bool ok;
+  if (L.key_fp8) ok = launch_shape<kFp8>(L.tile_bytes, group, &sh);
+  else if (L.key_bits == 4) ok = launch_shape<kMse4>(L.tile_bytes, group, &sh);
+  else ok = launch_shape<kMse3>(L.tile_bytes, group, &sh);
+  return ok ? sh.warps : 0;
 }
 
 tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* q, int q_dtype,
@@ -948,12 +1061,13 @@ tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* 
   a.max_seq_len = max_seq_len;
   a.cap = P.cap;
   a.tile_bytes = P.L.tile_bytes;
-  a.tile_stride = 0;
+  a.stage_bytes = 0;
   a.k_off = P.L.k_off;
   a.v_off = P.L.v_off;
   a.knorm_off = P.L.knorm_off;
   a.vscale_off = P.L.vscale_off;
   a.vzero_off = P.L.vzero_off;
+  a.qbuf_bytes = 0;
   a.warp_bytes = 0;
   a.dyn_bytes = 0;
   const float sm_scale = scale > 0.f ? scale : 0.088388347648318440f;   // 1/sqrt(128)
@@ -981,8 +1095,10 @@ tq_status run_reduce(const tq_config* cfg, const int* seq_lens, int batch, int m
   if (!aligned16(out) || !aligned16(workspace)) return TQ_ERR_MISALIGNED;
   make_plan(cfg, batch, max_seq_len, bt_stride, true, &P);
   if (P.sms <= 0) return TQ_ERR_CUDA;
-  ReduceArgs r;
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
+  const int warps = split_warps_per_cta(P.L, G);
+  if (warps <= 0) return TQ_ERR_CUDA;
+  ReduceArgs r;
   r.seq_lens = seq_lens;
   r.rec_o = static_cast<const float*>(workspace);
   r.rec_lse = r.rec_o + P.num_records * G * kD;
@@ -995,7 +1111,7 @@ tq_status run_reduce(const tq_config* cfg, const int* seq_lens, int batch, int m
   r.num_parts = P.num_parts;
   r.max_seq_len = max_seq_len;
   r.cap = P.cap;
-  r.num_warps = P.num_warps;
+  r.num_warps = P.sms * warps;
   const dim3 grid(static_cast<unsigned>(cfg->num_q_heads), static_cast<unsigned>(batch));
   if (out_dtype == TQ_DTYPE_F32) reduce_kernel<float><<<grid, kD, 0, stream>>>(r);
   else if (out_dtype == TQ_DTYPE_F16) reduce_kernel<__half><<<grid, kD, 0, stream>>>(r);

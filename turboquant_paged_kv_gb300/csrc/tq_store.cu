@@ -196,9 +196,12 @@ store_kernel(const StoreArgs a) {
     q = min(max(q, 0), 15);
     w |= static_cast<uint32_t>(q) << (4 * j);
   }
-  // pair-interleaved 16-bit words: word `lane` of token r
-  *reinterpret_cast<uint16_t*>(tile + a.v_off + (r >> 1) * 2 * a.v_row + 4 * lane + 2 * (r & 1)) =
-      static_cast<uint16_t>(w);
+  // pair-interleaved 16-bit words, 16-byte groups swizzled by the pair index:
+  // word `lane` of token r = 2p + j
+  const int pair = r >> 1;
+  const int swz = (a.v_row % 64 == 0) ? 2 * (pair & 3) : 0;
+  *reinterpret_cast<uint16_t*>(tile + a.v_off + pair * 2 * a.v_row + 16 * ((lane >> 2) ^ swz) + 4 * (lane & 3) +
+                               2 * (r & 1)) = static_cast<uint16_t>(w);
   if (lane == 0) {
     *reinterpret_cast<uint16_t*>(tile + a.vscale_off + 2 * r) = __half_as_ushort(__float2half_rn(s));
     *reinterpret_cast<uint16_t*>(tile + a.vzero_off + 2 * r) = __half_as_ushort(__float2half_rn(mn));

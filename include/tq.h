@@ -207,6 +207,39 @@ tq_status tq_decode_reduce(const tq_config* cfg, const int* seq_lens, int batch,
                            const void* workspace, size_t workspace_bytes,
                            tq_stream_t stream);
 
+/* Device. tq_decode with no workspace argument: the same kernels, the same
+ * result, with the workspace taken from a fixed array of
+ * TQ_DECODE_NOALLOC_SCRATCH_BYTES that this library holds in device memory
+ * (one copy per device). The method's description has no counterpart to this
+ * call; it is an addition of this library for callers that cannot allocate
+ * device memory: a plain C host with no device allocator of its own, or a
+ * serving loop that must not call cudaMalloc between steps (cudaMalloc can
+ * synchronise the device and can fail under memory pressure). Neither this
+ * call nor the kernels it launches allocate host or device memory.
+ *   Arguments, layouts and device-side errors are those of tq_decode.
+ *   Limit: returns TQ_ERR_WORKSPACE_TOO_SMALL, launching nothing, when
+ *   tq_decode_workspace_size(cfg, batch, max_seq_len) exceeds
+ *   TQ_DECODE_NOALLOC_SCRATCH_BYTES (e.g. more than about 12,000 (sequence,
+ *   KV head, partition) triples at 4 query heads per KV head).
+ *   Set-up: the first call on each device (the one current at the call)
+ *   looks the array's address up, which loads this part of the library on
+ *   that device; make that first call before any stream capture. A failed
+ *   look-up returns TQ_ERR_CUDA and is retried on the next call.
+ *   Initial contents: nothing in the array needs to start at zero; each call
+ *   writes every partial it later reads.
+ *   Concurrency: all calls on one device share the one array, so two calls
+ *   whose kernels may overlap (different streams, or different host threads
+ *   without ordering between their streams) race and give wrong results.
+ *   Calls on one stream run in order and are safe. */
+#define TQ_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+tq_status tq_decode_noalloc(const tq_config* cfg, const tq_codebook* cb,
+                            const void* q, int q_dtype,
+                            const void* cache, long long num_blocks,
+                            const int* block_table, int bt_stride,
+                            const int* seq_lens, int batch, int max_seq_len, float scale,
+                            void* out, int out_dtype,
+                            unsigned int* dev_status, tq_stream_t stream);
+
 /* Host. Static description of a status code. */
 const char* tq_status_string(int status);
 

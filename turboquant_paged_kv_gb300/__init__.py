@@ -15,7 +15,8 @@ import torch
 
 from . import _abi
 from ._abi import (PRESET_IDS, TQ_DEV_BLOCK_OUT_OF_RANGE, TQ_DEV_SEQ_TOO_LONG,  # noqa: F401
-                   TQ_DEV_SLOT_OUT_OF_RANGE, TQ_DTYPE_BF16, TQ_DTYPE_F16, TQ_DTYPE_F32,
+                   TQ_DECODE_NOALLOC_SCRATCH_BYTES, TQ_DEV_SLOT_OUT_OF_RANGE, TQ_DEV_TIMEOUT,
+                   TQ_DTYPE_BF16, TQ_DTYPE_F16, TQ_DTYPE_F32, TQ_ERR_WORKSPACE_TOO_SMALL,
                    TQError, tq_codebook, tq_config, tq_layout)
 
 
@@ -32,7 +33,8 @@ _LIB = _LazyLib()
 _DTYPES = {torch.float16: TQ_DTYPE_F16, torch.bfloat16: TQ_DTYPE_BF16, torch.float32: TQ_DTYPE_F32}
 
 __all__ = ["make_config", "tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode",
-           "tq_decode_partials", "tq_decode_reduce", "tq_decode_workspace_size", "tq_status_string",
+           "tq_decode_partials", "tq_decode_reduce", "tq_decode_noalloc", "tq_decode_workspace_size",
+           "tq_status_string",
            "tq_version", "TQError", "lib_path"]
 
 
@@ -109,6 +111,22 @@ def tq_decode(cfg: tq_config, cb, q: torch.Tensor, cache: torch.Tensor, block_ta
         _ptr(block_table), block_table.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, float(scale),
         _ptr(out), _DTYPES[out.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream)))
+
+
+def tq_decode_noalloc(cfg: tq_config, cb, q: torch.Tensor, cache: torch.Tensor, block_table: torch.Tensor,
+                      seq_lens: torch.Tensor, max_seq_len: int, out: torch.Tensor, scale: float = 0.0,
+                      num_blocks: int | None = None, dev_status: torch.Tensor | None = None,
+                      stream=None) -> None:
+    """tq_decode without a workspace argument: the library's fixed device array
+    of TQ_DECODE_NOALLOC_SCRATCH_BYTES serves as workspace (calls whose kernels
+    may overlap race on it; the first call on a device does the set-up)."""
+    lay = tq_layout_for(cfg)
+    if num_blocks is None:
+        num_blocks = cache.numel() // lay.block_bytes
+    _abi.check("tq_decode_noalloc", _LIB.tq_decode_noalloc(
+        ctypes.byref(cfg), _cb(cb), _ptr(q), _DTYPES[q.dtype], _ptr(cache), num_blocks,
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, float(scale),
+        _ptr(out), _DTYPES[out.dtype], _ptr(dev_status), _stream(stream)))
 
 
 def tq_decode_partials(cfg: tq_config, cb, q: torch.Tensor, cache: torch.Tensor, block_table: torch.Tensor,

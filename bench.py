@@ -330,7 +330,7 @@ def run_tq(args):
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16 mma / f32 accumulate over 4-bit codes", "data": "synthetic",
             "config": {"workload": f"{WORKLOAD}: {w.note}, d {w.d}, block {w.block_size}, {w.preset}, bf16 in/out",
-                       "partition_tokens": args.partition or 512,
+                       "partition_tokens": args.partition, "split": "stream-K: equal tile ranges per warp" if args.partition == 0 else "fixed partitions",
                        "l2": "3 rotated cache copies of %.0f MB each (> L2)" % (caches[0].numel() / 1e6),
                        "kv_bytes_per_step": kv_bytes},
             "decode_tok_s": world * B / (step_ms * 1e-3),

@@ -22,15 +22,18 @@
 //  segment + warp, which is unique because both sequences are monotone. Every
 //  warp does the same amount of work whatever the sequence lengths are.
 //
-//  Data movement. Each warp owns a ring of 2 stages in shared memory, each a
-//  chunk of up to 4 consecutive tiles (64 positions) of one segment, fed by
-//  cp.async.bulk (one 2144-byte copy per tile at 4bit_nc, all completing on the
-//  stage's mbarrier), and two query buffers fed the same way; the ring runs
-//  ahead across segment boundaries. Per-chunk work (waits, the softmax max,
-//  the rescale vote) is amortised over 64 positions and the 4 tiles give the
-//  tensor pipe 4 independent accumulation chains. Block ids are read 32 at a time into a lane-indexed
-//  register window. Every mbarrier wait is bounded: on expiry the warp flags
-//  TQ_DEV_TIMEOUT, drains its own copies (bounded again) and stops.
+//  Data movement. One CTA per SM: a producer warp and up to 10 consumer
+//  warps. Producer lane j walks consumer j's range chunk by chunk (a chunk is
+//  up to 2 consecutive tiles of one segment), reads block ids one chunk ahead,
+//  and fills consumer j's ring of 3 stages: a 16-byte descriptor (segment,
+//  first position, length, tile count, valid mask, last/new-segment bits), the
+//  tiles by cp.async.bulk (one 2144-byte copy per tile at 4bit_nc) and the
+//  segment's query rows when the chunk opens a segment, all completing on the
+//  stage's "full" mbarrier. Consumers only read descriptors and compute, and
+//  release a stage through its "empty" mbarrier. Every wait is bounded: a
+//  consumer whose wait expires flags TQ_DEV_TIMEOUT and stops; the producer
+//  gives up after a long stretch without progress and, in every case, waits
+//  (bounded) for all copies it issued before it leaves.
 //
 //  Math. Both contractions run on tensor cores with mma.sync.m16n8k16 (f16 in,
 //  f32 accumulate; one such mma occupies a sub-partition's tensor pipe for
@@ -40,10 +43,12 @@
 //      per key byte (32 copies, one per lane, so lookups never conflict; the
 //      table is aligned so one PRMT forms the address) is exactly the (row g,
 //      row 8 + g) operand pair, and the two rows are summed in the same lane.
-//      Columns hold q_hi of the G <= 4 query heads and q_lo of the same heads
-//      (q = q_hi + q_lo), so one mma per 16 coordinates covers all products to
-//      ~2^-22 relative (fp16 operands alone miss the 2e-3 output gate). For
-//      G > 4 the q_lo columns take a second mma.
+//      Columns 0..3 hold q_hi of the G <= 4 query heads and columns 4..7 q_lo of
+//      the same heads (q = q_hi + q_lo), so one mma per 16 coordinates covers
+//      all products to ~2^-22 relative (fp16 operands alone miss the 2e-3
+//      output gate), and lanes c, c ^ 2 of a quad hold the hi and lo parts of
+//      the same heads: one exchange completes the score. For G > 4 the q_lo
+//      columns take a second mma.
 //    P^T reaches the B-operand layout through movmatrix.trans (the S layout has
 //      tokens in rows), one instruction per 8x8 block of fp16 hi or lo parts.
 //    O^T[16 d x 8] = V^T[16 d x 16 tok] . P^T. The store interleaves the 16-bit
@@ -52,11 +57,13 @@
 //      subnormals (code * 2^-24, or code * 2^-20), so value operands cost one
 //      LOP3 per pair; the per-row power of two is removed at the end. The
 //      16-byte groups of the V region are XOR-swizzled by the pair index so
-//      these loads are free of bank conflicts. Columns
-//      carry hi and lo parts of p * scale; sum_p p * zero is kept on the side.
+//      these loads are free of bank conflicts. Columns carry the hi part of
+//      p * scale (lanes c < 2) or its lo part (lanes c >= 2, G <= 4), so both
+//      come out of one mma; sum_p p * zero is kept on the side.
 //  Softmax in log2 units with a lazy rescale: the running max of a head only
 //  moves when it grows by more than 2^8, decided by a warp vote, so rescaling
-//  the accumulators is off the common path.
+//  the accumulators is off the common path. The max starts at -1e30 (not
+//  -inf), so masked positions give exp2(-inf) = 0 without a guard.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -73,17 +80,22 @@ namespace {
 
 constexpr int kD = 128;
 #ifndef TQ_DECODE_WARPS
-#define TQ_DECODE_WARPS 8
+#define TQ_DECODE_WARPS 10
 #endif
-constexpr int kMaxWarps = TQ_DECODE_WARPS;   // warps per CTA (fewer when shared memory is short)
-constexpr int kChunk = 4;               // tiles per ring stage (64 tokens)
-constexpr int kStages = 2;              // ring stages per warp
+constexpr int kMaxConsumers = TQ_DECODE_WARPS;   // consumer warps per CTA (fewer when shared memory is short)
+constexpr int kChunk = 2;               // tiles per ring stage (32 positions)
+constexpr int kStages = 3;              // ring stages per consumer warp
+constexpr uint32_t kBarBytes = 512;     // mbarrier block at the start of shared memory
 constexpr float kTau = 8.0f;            // lazy rescale threshold, log2 units
 constexpr uint32_t kWaitLimit = 1u << 16;
 constexpr uint32_t kSuspendNs = 20000;  // try_wait suspend hint: bound ~ kWaitLimit * 20 us
+constexpr int kProducerSpin = 1 << 21;  // producer polls without progress before it gives up
 constexpr int kMaxCtas = 256;           // grid cap; sizes the workspace without a device query
-constexpr int kRecordWarps = 16;        // warps per CTA the workspace allows for (>= kMaxWarps)
-static_assert(kMaxWarps <= kRecordWarps, "workspace sized for at most 16 warps per CTA");
+constexpr int kRecordWarps = 16;        // consumer warps per CTA the workspace allows for
+static_assert(kMaxConsumers <= kRecordWarps, "workspace sized for at most 16 consumer warps per CTA");
+static_assert(kMaxConsumers <= 32, "one producer lane per consumer warp");
+static_assert(2 * kMaxConsumers * kStages * 8 <= static_cast<int>(kBarBytes), "barrier block too small");
+static_assert(kStages >= 2 && kStages <= 3, "consumer stage select handles 2 or 3 stages");
 
 enum KeyMode { kMse4 = 4, kMse3 = 3, kFp8 = 8 };
 
@@ -101,9 +113,10 @@ struct DecodeArgs {
   int part_tiles;      // tiles per partition (0: whole sequence)
   int num_parts;       // partitions per (b, h) in the record index
   int max_seq_len, cap;
-  int tile_bytes, stage_bytes, k_off, v_off, knorm_off, vscale_off, vzero_off;
+  int tile_bytes, k_off, v_off, knorm_off, vscale_off, vzero_off;
+  int stage_bytes;     // ring stage: kChunk tiles, query rows, descriptor
+  int q_off, desc_off; // offsets of the query rows and the descriptor in a stage
   int qbuf_bytes;      // G * d * 2
-  int warp_bytes;      // per-warp shared buffer
   int dyn_bytes;
   float qscale;        // softmax scale * log2(e)
   float cent[16];
@@ -157,9 +170,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
@@ -297,102 +307,66 @@ __device__ __forceinline__ uint32_t lut_addr(const uint4& kq, int s, uint32_t lu
   }
 }
 
-// ---------------------------------------------------------------- tile walker
+// ---------------------------------------------------------------- ring plan
 
-// Position in the (b, h, t) tile line. All fields are warp-uniform.
-struct Walk {
-  int b, h, t;      // sequence, KV head, tile within the sequence
-  int nt;           // tiles of sequence b
-  int len;          // clamped length of sequence b
-  int lens_base;    // first sequence of the lane-cached length window
-  int lens_reg;     // lane j: clamped length of sequence lens_base + j
-};
+// Address of ring stage `idx` (consumer j's stage s is idx = j * kStages + s):
+// stages are packed from `first` on and skip over the LUT, which sits at an
+// address aligned to its own size.
+__host__ __device__ __forceinline__ uint32_t stage_at(uint32_t first, uint32_t lut, uint32_t klut,
+                                                      uint32_t sb, int idx) {
+  if (klut) {
+    const uint32_t nb = lut > first ? (lut - first) / sb : 0u;
+    if (static_cast<uint32_t>(idx) >= nb) return lut + klut + (static_cast<uint32_t>(idx) - nb) * sb;
+  }
+  return first + static_cast<uint32_t>(idx) * sb;
+}
+
+__host__ __device__ __forceinline__ uint32_t lut_at(uint32_t base, uint32_t klut) {
+  return (base + kBarBytes + klut - 1) & ~(klut - 1);
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
 
 __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int len) {
   return min(max(len, 0), min(a.max_seq_len, a.cap));
 }
 
-__device__ __forceinline__ void lens_fill(Walk& w, const DecodeArgs& a, int base, int lane) {
-  w.lens_base = base;
-  const int j = base + lane;
-  w.lens_reg = j < a.batch ? clamp_len(a, __ldg(a.seq_lens + j)) : 0;
+// Barriers: consumer j, stage s: full at bars + 16 * (j * kStages + s), empty 8 after.
+__device__ __forceinline__ uint32_t full_bar(uint32_t bars, int j, int s) {
+  return bars + 16u * static_cast<uint32_t>(j * kStages + s);
 }
 
-__device__ __forceinline__ int lens_get(Walk& w, const DecodeArgs& a, int b, int lane) {
-  if (b - w.lens_base >= 32 || b < w.lens_base) lens_fill(w, a, b, lane);
-  return __shfl_sync(0xffffffffu, w.lens_reg, b - w.lens_base);
-}
+// ---------------------------------------------------------------- producer warp
 
-// Move to the next tile; skips empty sequences. Returns false past the end.
-__device__ __forceinline__ bool walk_next(Walk& w, const DecodeArgs& a, int lane) {
-  if (++w.t < w.nt) return true;
-  w.t = 0;
-  if (++w.h < a.n_kv) return true;
-  w.h = 0;
-  while (++w.b < a.batch) {
-    w.len = lens_get(w, a, w.b, lane);
-    w.nt = (w.len + kTileTokens - 1) / kTileTokens;
-    if (w.nt > 0) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ int segment_of(const Walk& w, const DecodeArgs& a) {
-  const int p = a.part_tiles > 0 ? w.t / a.part_tiles : 0;
-  return (w.b * a.n_kv + w.h) * a.num_parts + p;
-}
-
-// ---------------------------------------------------------------- split kernel
-
-// One consumer step handles a chunk of up to kChunk consecutive tiles of one
-// segment, held in one ring stage.
-template <int KMODE, int GBIG, typename TQ>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1)
-split_kernel(const DecodeArgs a) {
-  extern __shared__ __align__(1024) uint8_t s_dyn[];
+// Lane j < W feeds consumer warp j of this CTA: it walks that warp's range of
+// the tile line chunk by chunk (a chunk is up to kChunk consecutive tiles of
+// one segment), reads the chunk's block ids one chunk ahead, and for each
+// chunk fills the next free ring stage: a 16-byte descriptor
+// {segment, first position, sequence length, n | valid mask << 4 | last << 8 |
+// new segment << 9}, the tiles by cp.async.bulk, and the segment's query rows
+// when the chunk opens a segment. A consumer whose range is empty gets one
+// descriptor with n = 0 and the last bit.
+__device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_t first, uint32_t lut,
+                              uint32_t klut) {
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int nwarp_cta = blockDim.x >> 5;
-  const int g = lane >> 2;          // mma groupID
-  const int c = lane & 3;           // thread in group
-  const int G = a.group;
+  const bool mine = lane < W;
+  const long long nw = static_cast<long long>(gridDim.x) * W;
+  const long long wid = static_cast<long long>(blockIdx.x) * W + lane;
 
-  // ---- shared-memory plan: LUT at an address aligned to its size, warp
-  // buffers packed around it (identical in every thread)
-  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(s_dyn));
-  const uint32_t end = base + static_cast<uint32_t>(a.dyn_bytes);
-  constexpr uint32_t kLut = lut_bytes<KMODE>();
-  const uint32_t lut = kLut ? ((base + kLut - 1) & ~(kLut - 1)) : end;
-  uint32_t wbase = base, my_base = 0;
-  for (int w = 0; w <= warp; ++w) {
-    if (kLut && wbase < lut + kLut && wbase + a.warp_bytes > lut) wbase = lut + kLut;
-    if (w == warp) my_base = wbase;
-    wbase += a.warp_bytes;
-  }
-  const bool fits = my_base + a.warp_bytes <= end && (!kLut || lut + kLut <= end);
-  if (!__syncthreads_and(fits)) {   // launch misconfigured: flag and leave
-    if (threadIdx.x == 0) flag(a.status, TQ_DEV_TIMEOUT);
-    return;
-  }
-  if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent);
-
-  const uint32_t ring = my_base;                                  // kStages chunks
-  const uint32_t qbuf = ring + kStages * a.stage_bytes;           // 2 query buffers
-  const uint32_t bars = qbuf + 2 * a.qbuf_bytes;                  // kStages + 2 mbarriers
-  if (lane == 0) {
-    for (int i = 0; i < kStages + 2; ++i) mbar_init(bars + 8 * i, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  }
-  __syncthreads();   // LUT built, barriers initialised
-
-  uint32_t lut_lane = 0;
-  if constexpr (kLut != 0) lut_lane = lut + 8u * lane;
-  const uint64_t policy = evict_first_policy();
-
-  // ---- this warp's range of the tile line
-  const long long nwarps = static_cast<long long>(gridDim.x) * nwarp_cta;
-  const int wid = blockIdx.x * nwarp_cta + warp;
-  long long total = 0;   // n_kv * sum_b ceil(len_b / 16)
+  // tiles of the whole line: n_kv * sum_b ceil(len_b / 16)
+  long long total = 0;
   bool too_long = false;
   for (int b0 = 0; b0 < a.batch; b0 += 32) {
     const int j = b0 + lane;
@@ -405,48 +379,183 @@ split_kernel(const DecodeArgs a) {
     for (int o_ = 1; o_ < 32; o_ <<= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o_);
     total += nt;
   }
-  if (wid == 0 && __any_sync(0xffffffffu, too_long) && lane == 0) flag(a.status, TQ_DEV_SEQ_TOO_LONG);
+  if (blockIdx.x == 0 && __any_sync(0xffffffffu, too_long) && lane == 0) flag(a.status, TQ_DEV_SEQ_TOO_LONG);
   total *= a.n_kv;
-  const long long r0 = total * wid / nwarps;
-  const int ntiles = static_cast<int>(total * (wid + 1) / nwarps - r0);
-  if (ntiles <= 0) return;
+  const long long r0 = mine ? total * wid / nw : 0;
+  long long rem = mine ? total * (wid + 1) / nw - r0 : 0;
 
-  Walk pw;   // producer cursor: locate tile r0
+  // cursor: first tile of this lane's range, found for all lanes together over
+  // groups of 32 sequences
+  int cb = 0, ch = 0, ct = 0, cnt = 0, clen = 0;
   {
-    long long acc = 0;
-    int b = 0;
-    lens_fill(pw, a, 0, lane);
-    for (;;) {
-      const int len = lens_get(pw, a, b, lane);
+    bool found = rem <= 0;
+    long long acc = 0;   // tiles before the group
+    for (int b0 = 0; b0 < a.batch && __any_sync(0xffffffffu, !found); b0 += 32) {
+      const int bb = b0 + lane;
+      const int len = bb < a.batch ? clamp_len(a, __ldg(a.seq_lens + bb)) : 0;
       const int nt = (len + kTileTokens - 1) / kTileTokens;
       const long long span = static_cast<long long>(nt) * a.n_kv;
-      if (r0 < acc + span) {
-        const int off = static_cast<int>(r0 - acc);
-        pw.b = b; pw.len = len; pw.nt = nt;
-        pw.h = off / nt;
-        pw.t = off - pw.h * nt;
-        break;
+      long long inc = span;
+      for (int o_ = 1; o_ < 32; o_ <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, inc, o_);
+        if (lane >= o_) inc += y;
       }
-      acc += span;
-      ++b;
+      const long long excl = acc + inc - span;
+      for (int k = 0; k < W; ++k) {
+        if (!__shfl_sync(0xffffffffu, static_cast<int>(!found), k)) continue;
+        const long long x = __shfl_sync(0xffffffffu, r0, k);
+        const int idx = __popc(__ballot_sync(0xffffffffu, bb < a.batch && excl + span <= x));
+        if (idx < 32 && b0 + idx < a.batch) {
+          const long long e = __shfl_sync(0xffffffffu, excl, idx & 31);
+          const int n_t = __shfl_sync(0xffffffffu, nt, idx & 31);
+          const int ln = __shfl_sync(0xffffffffu, len, idx & 31);
+          if (lane == k) {
+            found = true;
+            cb = b0 + idx;
+            const int off = static_cast<int>(x - e);
+            ch = off / n_t;
+            ct = off - ch * n_t;
+            cnt = n_t;
+            clen = ln;
+          }
+        }
+      }
+      acc += __shfl_sync(0xffffffffu, inc, 31);
     }
   }
-  Walk cw = pw;   // consumer cursor
 
-  int bid_b = -1, bid_base = 0, bid_reg = 0;   // producer block-id window
-  int pi = 0, ci = 0;                           // tiles issued / consumed (relative to r0)
-  int p_stage = 0, c_stage = 0;
-  uint32_t c_phase = 0;                         // parity bit per stage, consumer side
-  uint32_t ok_bits = 0;                         // per stage, kChunk bits: tile copied
-  uint32_t stage_busy = 0;                      // per stage: issued, not yet consumed
-  int p_seg = -1, c_seg = -1;
-  int p_qslot = 1, c_qslot = 1;
-  uint32_t q_phase = 0, q_pending = 0;
-  bool p_done = false, aborted = false;
+  // the next chunk to issue (planned one chunk ahead, block ids in flight)
+  int n_n = 0, n_seg = 0, n_len = 0, n_b = 0, n_h = 0, n_t = 0;
+  int n_blk[kChunk];
+#pragma unroll
+  for (int i = 0; i < kChunk; ++i) n_blk[i] = -1;
+  auto plan = [&]() {
+    int n = min(kChunk, cnt - ct);
+    if (rem < n) n = static_cast<int>(rem);
+    if (a.part_tiles > 0) n = min(n, a.part_tiles - ct % a.part_tiles);
+    n_n = n;
+    n_b = cb;
+    n_h = ch;
+    n_t = ct;
+    n_len = clen;
+    n_seg = (cb * a.n_kv + ch) * a.num_parts + (a.part_tiles > 0 ? ct / a.part_tiles : 0);
+    const int* row = a.block_table + static_cast<long long>(cb) * a.bt_stride;
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) n_blk[i] = i < n ? __ldg(row + (((ct + i) << 4) >> a.log2_bs)) : -1;
+    rem -= n;
+    ct += n;
+    if (ct == cnt && rem > 0) {   // next (sequence, head); skip empty sequences
+      ct = 0;
+      if (++ch == a.n_kv) {
+        ch = 0;
+        do {
+          ++cb;
+          clen = clamp_len(a, __ldg(a.seq_lens + cb));
+          cnt = (clen + kTileTokens - 1) / kTileTokens;
+        } while (cnt == 0);
+      }
+    }
+  };
+  if (mine && rem > 0) plan();
+
+  const uint64_t policy = evict_first_policy();
+  uint32_t eparity = (1u << kStages) - 1;   // empty-barrier parity to wait for, per stage
+  uint32_t used = 0, fpar = 0;              // stages ever filled; parity of their next fill
+  int ps = 0, prev_seg = -1;
+  bool done = !mine;
+  int idle = 0;
+  while (__any_sync(0xffffffffu, !done)) {
+    bool progressed = false;
+    if (!done) {
+      const uint32_t fb = full_bar(bars, lane, ps);
+      if (mbar_test(fb + 8, (eparity >> ps) & 1u)) {
+        eparity ^= 1u << ps;
+        const uint32_t sa = stage_at(first, lut, klut, a.stage_bytes, lane * kStages + ps);
+        const bool last = rem <= 0;
+        const bool newq = n_n > 0 && n_seg != prev_seg;
+        uint32_t okm = 0, bytes = 0;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i)
+          if (i < n_n && n_blk[i] >= 0 && n_blk[i] < a.num_blocks) {
+            okm |= 1u << i;
+            bytes += a.tile_bytes;
+          }
+        if (newq) bytes += a.qbuf_bytes;
+        sts128(sa + a.desc_off, make_uint4(static_cast<uint32_t>(n_seg), static_cast<uint32_t>(n_t << 4),
+                                           static_cast<uint32_t>(n_len),
+                                           static_cast<uint32_t>(n_n) | (okm << 4) | (last ? 256u : 0u) |
+                                               (newq ? 512u : 0u)));
+        fence_proxy_async();
+        mbar_expect(fb, bytes);
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i)
+          if ((okm >> i) & 1u) {
+            const uint8_t* src = a.cache + ((static_cast<long long>(n_blk[i]) * a.n_kv + n_h) * a.tiles_per_block +
+                                            ((n_t + i) & (a.tiles_per_block - 1))) *
+                                               static_cast<long long>(a.tile_bytes);
+            bulk_g2s(sa + i * a.tile_bytes, src, a.tile_bytes, fb, policy);
+          }
+        if (newq) {
+          const uint8_t* src = static_cast<const uint8_t*>(a.q) +
+                               (static_cast<long long>(n_b) * a.n_q + n_h * a.group) * (kD * 2);
+          bulk_g2s_plain(sa + a.q_off, src, a.qbuf_bytes, fb);
+        }
+        if (n_n > 0) prev_seg = n_seg;
+        used |= 1u << ps;
+        fpar ^= 1u << ps;
+        ps = ps + 1 == kStages ? 0 : ps + 1;
+        progressed = true;
+        if (last) done = true;
+        else plan();
+      }
+    }
+    if (__any_sync(0xffffffffu, progressed)) {
+      idle = 0;
+    } else if (++idle > kProducerSpin) {   // a consumer stopped taking stages
+      if (lane == 0) flag(a.status, TQ_DEV_TIMEOUT);
+      break;
+    } else {
+      __nanosleep(64);
+    }
+  }
+  // every copy this lane issued has landed before the warp leaves (bounded)
+  if (mine)
+    for (int s = 0; s < kStages; ++s)
+      if ((used >> s) & 1u) mbar_wait(full_bar(bars, lane, s), ((fpar >> s) & 1u) ^ 1u);
+}
+
+// ---------------------------------------------------------------- consumer warps
+
+// Consumer warp j: takes its ring stages in order and runs the attention math
+// on every tile. Column layout of the score and output tiles (8 columns):
+//   G <= 4: column k < 4 carries the hi part of head k, column 4 + k the lo
+//     part, so lanes c and c ^ 2 of a quad hold the two parts of heads
+//     2 (c & 1), 2 (c & 1) + 1 and one exchange gives both the full score.
+//   G > 4: column k is head k; the lo parts run in a second mma into the same
+//     accumulators.
+template <int KMODE, int GBIG, typename TQ>
+__device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, uint32_t first, uint32_t lut,
+                              uint32_t klut) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;   // mma groupID
+  const int c = lane & 3;    // thread in group
+  const int G = a.group;
+  const int wid = blockIdx.x * W + j;
+  const int hd0 = GBIG ? 2 * c : 2 * (c & 1);   // heads of this lane's columns: hd0, hd0 + 1
+  const bool lo_lane = !GBIG && c >= 2;
+  const bool colv0 = hd0 < G, colv1 = hd0 + 1 < G;
+  const bool colmask = GBIG ? G < 8 : G < 4;    // some columns carry no head
+  uint32_t lut_lane = 0;
+  if constexpr (KMODE != kFp8) lut_lane = lut + 8u * lane;
+  uint32_t stg[kStages];
+#pragma unroll
+  for (int s = 0; s < kStages; ++s) stg[s] = stage_at(first, lut, klut, a.stage_bytes, j * kStages + s);
 
   uint32_t qb[GBIG ? 32 : 16];     // Q^T B operands (per k-step; GBIG: hi then lo)
-  float o[8][4];                   // O^T accumulators, rows d, cols n = 2c, 2c+1
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
+  float o[8][4];                   // O^T accumulators, rows d, cols 2c, 2c+1
+  float m0 = -1e30f, m1 = -1e30f, l0 = 0.f, l1 = 0.f, z0 = 0.f, z1 = 0.f;
+  int c_seg = -1;
+  uint32_t fpar = 0;
 
   auto finalize = [&](int seg) {
     float l_[2] = {l0, l1}, z_[2] = {z0, z1};
@@ -461,372 +570,259 @@ split_kernel(const DecodeArgs a) {
     const int rec = seg + wid;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int n = 2 * c + e;
-      const int pc = n + G;                      // lo column of head n (G <= 4)
-      const int src = 4 * g + ((pc >> 1) & 3);
+      const int hd = hd0 + e;
+      const bool writer = hd < G && !lo_lane;
       const float inv = l_[e] > 0.f ? 1.f / l_[e] : 0.f;
-      float* dst = a.rec_o + (static_cast<long long>(rec) * G + (n < G ? n : 0)) * kD + 16 * g;
+      float* dst = a.rec_o + (static_cast<long long>(rec) * G + (writer ? hd : 0)) * kD + 16 * g;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         float v0 = o[mt][e], v1 = o[mt][2 + e];
-        if (!GBIG) {
-          v0 += __shfl_sync(0xffffffffu, o[mt][pc & 1], src);
-          v1 += __shfl_sync(0xffffffffu, o[mt][2 + (pc & 1)], src);
+        if (!GBIG) {   // add the lo-part columns held by lane ^ 2
+          v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+          v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
         }
         // value operands carried code * 2^-24 (rows g) and code * 2^-20 (rows g + 8)
-        if (n < G)
+        if (writer)
           *reinterpret_cast<float2*>(dst + 2 * mt) =
               make_float2(fmaf(v0, 16777216.f, z_[e]) * inv, fmaf(v1, 1048576.f, z_[e]) * inv);
       }
-      if (n < G && g == 0)
-        a.rec_lse[static_cast<long long>(rec) * G + n] = l_[e] > 0.f ? mm[e] + __log2f(l_[e]) : -INFINITY;
+      if (writer && g == 0)
+        a.rec_lse[static_cast<long long>(rec) * G + hd] = l_[e] > 0.f ? mm[e] + __log2f(l_[e]) : -INFINITY;
     }
   };
 
-  while (ci < ntiles) {
-    // ---------------- producer: fill free stages with chunks. A chunk is up
-    // to kChunk tiles of one segment; a new segment needs a free query buffer
-    // (the consumer must have begun the one before it).
-    while (!p_done && !((stage_busy >> p_stage) & 1u)) {
-      const int seg = segment_of(pw, a);
-      if (seg != p_seg) {
-        if (p_seg >= 0 && c_seg < p_seg) break;
-        p_qslot ^= 1;
-        q_pending |= 1u << p_qslot;
-        if (lane == 0) {
-          const uint32_t bar = bars + 8 * (kStages + p_qslot);
-          const uint8_t* src = static_cast<const uint8_t*>(a.q) +
-                               (static_cast<long long>(pw.b) * a.n_q + pw.h * G) * (kD * 2);
-          fence_proxy_async();
-          mbar_expect(bar, a.qbuf_bytes);
-          bulk_g2s_plain(qbuf + p_qslot * a.qbuf_bytes, src, a.qbuf_bytes, bar);
-        }
-        p_seg = seg;
-      }
-      const uint32_t bar = bars + 8 * p_stage;
-      if (lane == 0) fence_proxy_async();
-      uint32_t okm = 0;
-      int n = 0;
-      for (;;) {
-        const int blk_i = (pw.t << 4) >> a.log2_bs;   // block index within the sequence
-        if (pw.b != bid_b || blk_i - bid_base >= 32 || blk_i < bid_base) {
-          bid_b = pw.b;
-          bid_base = blk_i;
-          const int j = bid_base + lane;
-          bid_reg = (j * a.block_size < pw.len) ? __ldg(a.block_table + static_cast<long long>(pw.b) * a.bt_stride + j) : -1;
-        }
-        const int blk = __shfl_sync(0xffffffffu, bid_reg, blk_i - bid_base);
-        if (blk >= 0 && blk < a.num_blocks) {
-          okm |= 1u << n;
-          if (lane == 0) {
-            const uint8_t* src = a.cache + ((static_cast<long long>(blk) * a.n_kv + pw.h) * a.tiles_per_block +
-                                            (pw.t & (a.tiles_per_block - 1))) *
-                                               static_cast<long long>(a.tile_bytes);
-            mbar_expect_tx(bar, a.tile_bytes);
-            bulk_g2s(ring + p_stage * a.stage_bytes + n * a.tile_bytes, src, a.tile_bytes, bar, policy);
-          }
-        }
-        ++n;
-        ++pi;
-        if (pi >= ntiles || !walk_next(pw, a, lane)) { p_done = true; break; }
-        if (n == kChunk || segment_of(pw, a) != seg) break;
-      }
-      if (lane == 0) mbar_arrive(bar);
-      ok_bits = (ok_bits & ~(((1u << kChunk) - 1) << (kChunk * p_stage))) | (okm << (kChunk * p_stage));
-      stage_busy |= 1u << p_stage;
-      p_stage = p_stage + 1 == kStages ? 0 : p_stage + 1;
-    }
-
-    // ---------------- consumer
-    const int seg = segment_of(cw, a);
-    if (seg != c_seg) {
-      if (c_seg >= 0) finalize(c_seg);
-      // ---- begin the segment: its query rows, rotated, scaled, split hi/lo
-      c_qslot ^= 1;
-      if (!mbar_wait(bars + 8 * (kStages + c_qslot), (q_phase >> c_qslot) & 1u)) { aborted = true; break; }
-      q_phase ^= 1u << c_qslot;
-      q_pending &= ~(1u << c_qslot);
+  // query rows of a new segment: rotate, scale, split hi/lo, scatter into B operands
+  auto begin_segment = [&](uint32_t qrows) {
 #pragma unroll
-      for (int i = 0; i < (GBIG ? 32 : 16); ++i) qb[i] = 0u;
+    for (int i = 0; i < (GBIG ? 32 : 16); ++i) qb[i] = 0u;
 #pragma unroll
-      for (int gg = 0; gg < 8; ++gg) {
-        if (gg < G) {
-          float x[4];
-          u2_to_f4<TQ>(lds64(qbuf + c_qslot * a.qbuf_bytes + gg * kD * 2 + 8 * lane), x);
-          float sc = a.qscale;
-          if constexpr (KMODE != kFp8) {
-            fwht128(x, lane);
-            sc *= 0.088388347648318440f;   // 1 / sqrt(128)
-          }
-          uint32_t hp[4];   // hi01, lo01, hi23, lo23 of coordinates 4 lane .. +3
-          split_half2(x[0] * sc, x[1] * sc, hp[0], hp[1]);
-          split_half2(x[2] * sc, x[3] * sc, hp[2], hp[3]);
-          // B column g takes head gg's hi part (g == gg) or lo part (g == gg + G)
-          const bool take_hi = g == gg, take_lo = GBIG ? (g == gg) : (g == gg + G);
-          if constexpr (KMODE == kFp8) {
+    for (int gg = 0; gg < 8; ++gg) {
+      if (gg < G) {
+        float x[4];
+        u2_to_f4<TQ>(lds64(qrows + gg * kD * 2 + 8 * lane), x);
+        float sc = a.qscale;
+        if constexpr (KMODE != kFp8) {
+          fwht128(x, lane);
+          sc *= 0.088388347648318440f;   // 1 / sqrt(128)
+        }
+        uint32_t hp[4];   // hi01, lo01, hi23, lo23 of coordinates 4 lane .. +3
+        split_half2(x[0] * sc, x[1] * sc, hp[0], hp[1]);
+        split_half2(x[2] * sc, x[3] * sc, hp[2], hp[3]);
+        // B column g takes head gg's hi part (g == gg) or lo part (g == gg + 4)
+        const bool take_hi = g == gg, take_lo = GBIG ? (g == gg) : (g == gg + 4);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3 live in lane 8c + s
-              const uint32_t h01 = __shfl_sync(0xffffffffu, hp[0], 8 * c + s);
-              const uint32_t l01 = __shfl_sync(0xffffffffu, hp[1], 8 * c + s);
-              const uint32_t h23 = __shfl_sync(0xffffffffu, hp[2], 8 * c + s);
-              const uint32_t l23 = __shfl_sync(0xffffffffu, hp[3], 8 * c + s);
-              if (GBIG) {
-                if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; qb[16 + 2 * s] = l01; qb[16 + 2 * s + 1] = l23; }
-              } else {
-                if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; }
-                if (take_lo) { qb[2 * s] = l01; qb[2 * s + 1] = l23; }
-              }
-            }
+        for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3 live in lane 8c + s
+          const uint32_t h01 = __shfl_sync(0xffffffffu, hp[0], 8 * c + s);
+          const uint32_t l01 = __shfl_sync(0xffffffffu, hp[1], 8 * c + s);
+          const uint32_t h23 = __shfl_sync(0xffffffffu, hp[2], 8 * c + s);
+          const uint32_t l23 = __shfl_sync(0xffffffffu, hp[3], 8 * c + s);
+          if (GBIG) {
+            if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; qb[16 + 2 * s] = l01; qb[16 + 2 * s + 1] = l23; }
           } else {
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3 live in lane 8c + s
-              const uint32_t h01 = __shfl_sync(0xffffffffu, hp[0], 8 * c + s);
-              const uint32_t l01 = __shfl_sync(0xffffffffu, hp[1], 8 * c + s);
-              const uint32_t h23 = __shfl_sync(0xffffffffu, hp[2], 8 * c + s);
-              const uint32_t l23 = __shfl_sync(0xffffffffu, hp[3], 8 * c + s);
-              if (GBIG) {
-                if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; qb[16 + 2 * s] = l01; qb[16 + 2 * s + 1] = l23; }
-              } else {
-                if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; }
-                if (take_lo) { qb[2 * s] = l01; qb[2 * s + 1] = l23; }
-              }
-            }
+            if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; }
+            if (take_lo) { qb[2 * s] = l01; qb[2 * s + 1] = l23; }
           }
         }
       }
-      __syncwarp();   // query buffer fully read before the producer may reuse it
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-      m0 = m1 = -INFINITY;
-      l0 = l1 = z0 = z1 = 0.f;
-      c_seg = seg;
     }
-
-    // chunk of this stage: n tiles from cw (same rule as the producer)
-    int n = 1;
-    {
-      Walk t = cw;
-      while (n < kChunk && ci + n < ntiles && walk_next(t, a, lane) && segment_of(t, a) == seg) ++n;
-    }
-    if (!mbar_wait(bars + 8 * c_stage, (c_phase >> c_stage) & 1u)) { aborted = true; break; }
-    c_phase ^= 1u << c_stage;
-    const uint32_t okm = (ok_bits >> (kChunk * c_stage)) & ((1u << kChunk) - 1);
-    if (okm != (1u << n) - 1 && lane == 0) flag(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
-    const uint32_t st = ring + c_stage * a.stage_bytes;
-    const int tok0 = cw.t << 4;   // first position of the chunk in its sequence
-
-    // ---- S[i] = K_i . Q^T for the chunk's tiles (missing tiles compute on
-    // stale bytes and are masked below)
-    float S[kChunk][4];
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) S[i][0] = S[i][1] = S[i][2] = S[i][3] = 0.f;
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    m0 = m1 = -1e30f;
+    l0 = l1 = z0 = z1 = 0.f;
+  };
+
+  // one 16-token tile at shared address tb; nvalid of its positions are real
+  auto tile = [&](uint32_t tb, int nvalid) {
+    // ---- S = K . Q^T
+    float v[4];   // [0] tok g col 2c, [1] tok g col 2c+1, [2] tok g+8 col 2c, [3] tok g+8 col 2c+1
     if constexpr (KMODE == kFp8) {
+      float S[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t kt = tb + a.k_off;
+      const uint4 kg0 = lds128(kt + g * 128 + 32 * c), kg1 = lds128(kt + g * 128 + 32 * c + 16);
+      const uint4 kh0 = lds128(kt + (g + 8) * 128 + 32 * c), kh1 = lds128(kt + (g + 8) * 128 + 32 * c + 16);
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const uint32_t kt = st + i * a.tile_bytes + a.k_off;
-        const uint4 kg0 = lds128(kt + g * 128 + 32 * c), kg1 = lds128(kt + g * 128 + 32 * c + 16);
-        const uint4 kh0 = lds128(kt + (g + 8) * 128 + 32 * c), kh1 = lds128(kt + (g + 8) * 128 + 32 * c + 16);
-#pragma unroll
-        for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3
-          const uint32_t wg = word_of(s < 4 ? kg0 : kg1, s & 3), wh = word_of(s < 4 ? kh0 : kh1, s & 3);
-          const __half2_raw g01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wg & 0xFFFFu), __NV_E4M3);
-          const __half2_raw g23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wg >> 16), __NV_E4M3);
-          const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh & 0xFFFFu), __NV_E4M3);
-          const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh >> 16), __NV_E4M3);
-          const uint32_t a0 = static_cast<uint32_t>(g01.x) | (static_cast<uint32_t>(g01.y) << 16);
-          const uint32_t a1 = static_cast<uint32_t>(h01.x) | (static_cast<uint32_t>(h01.y) << 16);
-          const uint32_t a2 = static_cast<uint32_t>(g23.x) | (static_cast<uint32_t>(g23.y) << 16);
-          const uint32_t a3 = static_cast<uint32_t>(h23.x) | (static_cast<uint32_t>(h23.y) << 16);
-          mma16816(S[i], a0, a1, a2, a3, qb[2 * s], qb[2 * s + 1]);
-          if (GBIG) mma16816(S[i], a0, a1, a2, a3, qb[16 + 2 * s], qb[16 + 2 * s + 1]);
-        }
+      for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3
+        const uint32_t wg = word_of(s < 4 ? kg0 : kg1, s & 3), wh = word_of(s < 4 ? kh0 : kh1, s & 3);
+        const __half2_raw g01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wg & 0xFFFFu), __NV_E4M3);
+        const __half2_raw g23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wg >> 16), __NV_E4M3);
+        const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh & 0xFFFFu), __NV_E4M3);
+        const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh >> 16), __NV_E4M3);
+        const uint32_t a0 = static_cast<uint32_t>(g01.x) | (static_cast<uint32_t>(g01.y) << 16);
+        const uint32_t a1 = static_cast<uint32_t>(h01.x) | (static_cast<uint32_t>(h01.y) << 16);
+        const uint32_t a2 = static_cast<uint32_t>(g23.x) | (static_cast<uint32_t>(g23.y) << 16);
+        const uint32_t a3 = static_cast<uint32_t>(h23.x) | (static_cast<uint32_t>(h23.y) << 16);
+        mma16816(S, a0, a1, a2, a3, qb[2 * s], qb[2 * s + 1]);
+        if (GBIG) mma16816(S, a0, a1, a2, a3, qb[16 + 2 * s], qb[16 + 2 * s + 1]);
       }
+      v[0] = S[0]; v[1] = S[1]; v[2] = S[2]; v[3] = S[3];
     } else {
-      uint4 kg[kChunk], kh[kChunk];   // this lane's key slice of tokens g and g+8
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const uint32_t kt = st + i * a.tile_bytes + a.k_off;
-        if constexpr (KMODE == kMse4) {
-          kg[i] = lds128(kt + g * 64 + 16 * c);
-          kh[i] = lds128(kt + (g + 8) * 64 + 16 * c);
-        } else {
-          const uint32_t ra = kt + g * 48 + 12 * c, rb = kt + (g + 8) * 48 + 12 * c;
-          kg[i] = make_uint4(lds32(ra), lds32(ra + 4), lds32(ra + 8), 0u);
-          kh[i] = make_uint4(lds32(rb), lds32(rb + 4), lds32(rb + 8), 0u);
-        }
+      const uint32_t kt = tb + a.k_off;
+      uint4 kg, kh;   // this lane's key slice of tokens g and g+8
+      if constexpr (KMODE == kMse4) {
+        kg = lds128(kt + g * 64 + 16 * c);
+        kh = lds128(kt + (g + 8) * 64 + 16 * c);
+      } else {
+        const uint32_t ra = kt + g * 48 + 12 * c, rb = kt + (g + 8) * 48 + 12 * c;
+        kg = make_uint4(lds32(ra), lds32(ra + 4), lds32(ra + 8), 0u);
+        kh = make_uint4(lds32(rb), lds32(rb + 4), lds32(rb + 8), 0u);
       }
       // M rows: 8 tokens x {centroid hi part, centroid lo part}; k-step s holds
       // this lane's coordinates 32c + 4s .. +3 (two key bytes = two LUT entries,
       // each entry = the (hi, lo) operand pair of one row pair)
-      float Sl[kChunk][2][4];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) Sl[i][u][0] = Sl[i][u][1] = Sl[i][u][2] = Sl[i][u][3] = 0.f;
+      float Sg[4] = {0.f, 0.f, 0.f, 0.f}, Sh[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int s2 = 0; s2 < 8; ++s2) {
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-          const uint2 g0 = lds64(lut_addr<KMODE>(kg[i], 2 * s2, lut_lane));
-          const uint2 g1 = lds64(lut_addr<KMODE>(kg[i], 2 * s2 + 1, lut_lane));
-          const uint2 h0 = lds64(lut_addr<KMODE>(kh[i], 2 * s2, lut_lane));
-          const uint2 h1 = lds64(lut_addr<KMODE>(kh[i], 2 * s2 + 1, lut_lane));
-          mma16816(Sl[i][0], g0.x, g0.y, g1.x, g1.y, qb[2 * s2], qb[2 * s2 + 1]);
-          mma16816(Sl[i][1], h0.x, h0.y, h1.x, h1.y, qb[2 * s2], qb[2 * s2 + 1]);
-          if (GBIG) {
-            mma16816(Sl[i][0], g0.x, g0.y, g1.x, g1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
-            mma16816(Sl[i][1], h0.x, h0.y, h1.x, h1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
-          }
+        const uint2 g0 = lds64(lut_addr<KMODE>(kg, 2 * s2, lut_lane));
+        const uint2 g1 = lds64(lut_addr<KMODE>(kg, 2 * s2 + 1, lut_lane));
+        const uint2 h0 = lds64(lut_addr<KMODE>(kh, 2 * s2, lut_lane));
+        const uint2 h1 = lds64(lut_addr<KMODE>(kh, 2 * s2 + 1, lut_lane));
+        mma16816(Sg, g0.x, g0.y, g1.x, g1.y, qb[2 * s2], qb[2 * s2 + 1]);
+        mma16816(Sh, h0.x, h0.y, h1.x, h1.y, qb[2 * s2], qb[2 * s2 + 1]);
+        if (GBIG) {
+          mma16816(Sg, g0.x, g0.y, g1.x, g1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
+          mma16816(Sh, h0.x, h0.y, h1.x, h1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
         }
       }
       // rows g (hi part) + g + 8 (lo part) of each token: same lane
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        S[i][0] = Sl[i][0][0] + Sl[i][0][2];
-        S[i][1] = Sl[i][0][1] + Sl[i][0][3];
-        S[i][2] = Sl[i][1][0] + Sl[i][1][2];
-        S[i][3] = Sl[i][1][1] + Sl[i][1][3];
-      }
+      v[0] = Sg[0] + Sg[2];
+      v[1] = Sg[1] + Sg[3];
+      v[2] = Sh[0] + Sh[2];
+      v[3] = Sh[1] + Sh[3];
     }
 
-    // ---- scores: combine q_lo columns, norms, masks; per-head chunk max
-    // S[i]: [0] tok g col 2c, [1] tok g col 2c+1, [2] tok g+8 col 2c, [3] tok g+8 col 2c+1
-    float sv[kChunk][2], sz[kChunk][2];   // value scale / zero of tokens g, g+8
-    float cm0 = -INFINITY, cm1 = -INFINITY;
+    // ---- scores: q hi + lo columns, norms, masks
+    if (!GBIG) {
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      const uint32_t tb = st + i * a.tile_bytes;
-      float* v = S[i];
-      if (!GBIG) {   // add the q_lo column of each head (column + G)
-        const int srcA = 4 * g + (((2 * c + G) >> 1) & 3), srcB = 4 * g + (((2 * c + 1 + G) >> 1) & 3);
-        const bool odd = G & 1;
-        const float t0 = __shfl_sync(0xffffffffu, odd ? v[1] : v[0], srcA);
-        const float t2 = __shfl_sync(0xffffffffu, odd ? v[3] : v[2], srcA);
-        const float t1 = __shfl_sync(0xffffffffu, odd ? v[0] : v[1], srcB);
-        const float t3 = __shfl_sync(0xffffffffu, odd ? v[2] : v[3], srcB);
-        v[0] += t0; v[1] += t1; v[2] += t2; v[3] += t3;
-      }
-      if constexpr (KMODE != kFp8) {
-        const float ng = lds_h2f(tb + a.knorm_off + 2 * g), nh = lds_h2f(tb + a.knorm_off + 2 * g + 16);
-        v[0] *= ng; v[1] *= ng; v[2] *= nh; v[3] *= nh;
-      }
-      sv[i][0] = lds_h2f(tb + a.vscale_off + 2 * g);
-      sv[i][1] = lds_h2f(tb + a.vscale_off + 2 * g + 16);
-      sz[i][0] = lds_h2f(tb + a.vzero_off + 2 * g);
-      sz[i][1] = lds_h2f(tb + a.vzero_off + 2 * g + 16);
-      const int nvalid = ((okm >> i) & 1u) ? min(kTileTokens, cw.len - tok0 - 16 * i) : 0;
-      if (nvalid < kTileTokens) {   // missing or ragged tile
-        if (g >= nvalid) { v[0] = v[1] = -INFINITY; sv[i][0] = 0.f; sz[i][0] = 0.f; }
-        if (g + 8 >= nvalid) { v[2] = v[3] = -INFINITY; sv[i][1] = 0.f; sz[i][1] = 0.f; }
-      }
-      cm0 = fmaxf(cm0, fmaxf(v[0], v[2]));
-      cm1 = fmaxf(cm1, fmaxf(v[1], v[3]));
+      for (int k = 0; k < 4; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], 2);
     }
-#pragma unroll
-    for (int o_ = 4; o_ < 32; o_ <<= 1) {
-      cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, o_));
-      cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, o_));
+    if constexpr (KMODE != kFp8) {
+      const float ng = lds_h2f(tb + a.knorm_off + 2 * g), nh = lds_h2f(tb + a.knorm_off + 2 * g + 16);
+      v[0] *= ng; v[1] *= ng; v[2] *= nh; v[3] *= nh;
     }
-    const bool need = (2 * c < G && cm0 > m0 + kTau) || (2 * c + 1 < G && cm1 > m1 + kTau);
+    float svg = lds_h2f(tb + a.vscale_off + 2 * g), svh = lds_h2f(tb + a.vscale_off + 2 * g + 16);
+    float szg = lds_h2f(tb + a.vzero_off + 2 * g), szh = lds_h2f(tb + a.vzero_off + 2 * g + 16);
+    if (nvalid < kTileTokens) {   // missing or ragged tile
+      if (g >= nvalid) { v[0] = v[1] = -INFINITY; svg = 0.f; szg = 0.f; }
+      if (g + 8 >= nvalid) { v[2] = v[3] = -INFINITY; svh = 0.f; szh = 0.f; }
+    }
+    if (colmask) {
+      if (!colv0) v[0] = v[2] = -INFINITY;
+      if (!colv1) v[1] = v[3] = -INFINITY;
+    }
+    const bool need = fmaxf(v[0], v[2]) > m0 + kTau || fmaxf(v[1], v[3]) > m1 + kTau;
     if (__any_sync(0xffffffffu, need)) {   // rare: move the running max, rescale
+      float cm0 = fmaxf(v[0], v[2]), cm1 = fmaxf(v[1], v[3]);
+#pragma unroll
+      for (int o_ = 4; o_ < 32; o_ <<= 1) {
+        cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, o_));
+        cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, o_));
+      }
       float al0 = 1.f, al1 = 1.f;
       if (cm0 > m0 + kTau) { al0 = ex2(m0 - cm0); m0 = cm0; }
       if (cm1 > m1 + kTau) { al1 = ex2(m1 - cm1); m1 = cm1; }
       l0 *= al0; z0 *= al0; l1 *= al1; z1 *= al1;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {   // O^T column 2c + e belongs to head hn
-        const int nn = 2 * c + e;
-        const int hn = GBIG ? nn : (nn < G ? nn : (nn < 2 * G ? nn - G : 0));
-        const float x0 = __shfl_sync(0xffffffffu, al0, 4 * g + (hn >> 1));
-        const float x1 = __shfl_sync(0xffffffffu, al1, 4 * g + (hn >> 1));
-        const float al = (hn & 1) ? x1 : x0;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) { o[mt][e] *= al; o[mt][2 + e] *= al; }
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= al0; o[mt][2] *= al0;
+        o[mt][1] *= al1; o[mt][3] *= al1;
       }
     }
 
-    // ---- per tile: probabilities, P^T operands (movmatrix), O^T += V^T . P^T
+    // ---- probabilities, P^T operands (movmatrix), O^T += V^T . P^T
+    const float p0 = ex2(v[0] - m0), p1 = ex2(v[1] - m1);
+    const float p2 = ex2(v[2] - m0), p3 = ex2(v[3] - m1);
+    l0 += p0 + p2;
+    l1 += p1 + p3;
+    z0 = fmaf(p0, szg, fmaf(p2, szh, z0));
+    z1 = fmaf(p1, szg, fmaf(p3, szh, z1));
+    uint32_t hg, lg, hh, lh;   // hi/lo half2 of (col 2c, col 2c+1) for tokens g and g+8
+    split_half2(p0 * svg, p1 * svg, hg, lg);
+    split_half2(p2 * svh, p3 * svh, hh, lh);
+    const uint32_t b0 = movmatrix_trans(lo_lane ? lg : hg), b1 = movmatrix_trans(lo_lane ? lh : hh);
+    uint32_t b0l = 0u, b1l = 0u;
+    if (GBIG) { b0l = movmatrix_trans(lg); b1l = movmatrix_trans(lh); }
+    const uint32_t vt = tb + a.v_off + 16 * (g ^ (2 * c));
+    const uint4 va = lds128(vt + 128 * c);         // tokens 2c, 2c+1
+    const uint4 vb = lds128(vt + 128 * (c + 4));   // tokens 2c+8, 2c+9
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      const float* v = S[i];
-      // fmaxf also maps the NaN of (-inf) - (-inf) (a fully masked chunk before
-      // any valid position) to an argument whose exp2 is 0
-      const float p0 = ex2(fmaxf(v[0] - m0, -200.f)), p1 = ex2(fmaxf(v[1] - m1, -200.f));
-      const float p2 = ex2(fmaxf(v[2] - m0, -200.f)), p3 = ex2(fmaxf(v[3] - m1, -200.f));
-      l0 += p0 + p2;
-      l1 += p1 + p3;
-      z0 = fmaf(p0, sz[i][0], fmaf(p2, sz[i][1], z0));
-      z1 = fmaf(p1, sz[i][0], fmaf(p3, sz[i][1], z1));
-      uint32_t hg, lg, hh, lh;   // hi/lo half2 of (col 2c, col 2c+1) for tokens g and g+8
-      split_half2(p0 * sv[i][0], p1 * sv[i][0], hg, lg);
-      split_half2(p2 * sv[i][1], p3 * sv[i][1], hh, lh);
-      uint32_t mg, mh, mgl = 0u, mhl = 0u;   // P matrices [token][column] in mma layout
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t wa = word_of(va, k), wb = word_of(vb, k);
+      const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+      mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0, b1);
+      mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0, b1);
       if (GBIG) {
-        const uint32_t keep = (2 * c + 1 < G) ? 0xFFFFFFFFu : ((2 * c < G) ? 0x0000FFFFu : 0u);
-        mg = hg & keep; mh = hh & keep; mgl = lg & keep; mhl = lh & keep;
-      } else {
-        // column n < G: hi of head n (own); G <= n < 2G: lo of head n - G
-        uint32_t sel_g = 0u, sel_h = 0u;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int nn = 2 * c + e;
-          const int hn = nn - G;
-          const int src = 4 * g + ((hn >> 1) & 3);
-          const uint32_t wg = __shfl_sync(0xffffffffu, lg, src);
-          const uint32_t wh = __shfl_sync(0xffffffffu, lh, src);
-          uint32_t xg, xh;
-          if (nn < G) {
-            xg = e ? (hg >> 16) : (hg & 0xFFFFu);
-            xh = e ? (hh >> 16) : (hh & 0xFFFFu);
-          } else if (nn < 2 * G) {
-            xg = (hn & 1) ? (wg >> 16) : (wg & 0xFFFFu);
-            xh = (hn & 1) ? (wh >> 16) : (wh & 0xFFFFu);
-          } else {
-            xg = xh = 0u;
-          }
-          sel_g |= xg << (16 * e);
-          sel_h |= xh << (16 * e);
-        }
-        mg = sel_g;
-        mh = sel_h;
+        mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0l, b1l);
+        mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0l,
+                 b1l);
       }
-      const uint32_t b0 = movmatrix_trans(mg), b1 = movmatrix_trans(mh);
-      const uint32_t tb = st + i * a.tile_bytes + a.v_off + 16 * (g ^ (2 * c));
-      const uint4 va = lds128(tb + 128 * c);         // tokens 2c, 2c+1
-      const uint4 vb = lds128(tb + 128 * (c + 4));   // tokens 2c+8, 2c+9
-      uint32_t b0l = 0u, b1l = 0u;
-      if (GBIG) { b0l = movmatrix_trans(mgl); b1l = movmatrix_trans(mhl); }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t wa = word_of(va, k), wb = word_of(vb, k);
-        const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-        mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0, b1);
-        mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0, b1);
-        if (GBIG) {
-          mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0l, b1l);
-          mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0l,
-                   b1l);
-        }
+    }
+  };
+
+  int cs = 0;
+  bool aborted = false;
+  for (;;) {
+    const uint32_t fb = full_bar(bars, j, cs);
+    if (!mbar_wait(fb, (fpar >> cs) & 1u)) { aborted = true; break; }
+    fpar ^= 1u << cs;
+    const uint32_t sa = cs == 0 ? stg[0] : (cs == 1 ? stg[1] : stg[kStages - 1]);
+    const uint4 desc = lds128(sa + a.desc_off);
+    const int n = static_cast<int>(desc.w & 7u);
+    const uint32_t okm = (desc.w >> 4) & 0xFu;
+    const bool last = (desc.w >> 8) & 1u;
+    if (n > 0) {
+      const int seg = static_cast<int>(desc.x);
+      if (seg != c_seg) {
+        if (c_seg >= 0) finalize(c_seg);
+        begin_segment(sa + a.q_off);
+        c_seg = seg;
       }
+      const int tok0 = static_cast<int>(desc.y), len = static_cast<int>(desc.z);
+      if (okm != (1u << n) - 1 && lane == 0) flag(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i)
+        if (i < n) tile(sa + i * a.tile_bytes, ((okm >> i) & 1u) ? min(kTileTokens, len - tok0 - 16 * i) : 0);
     }
     __syncwarp();   // every lane has read the stage: the producer may refill it
-    stage_busy &= ~(1u << c_stage);
-    c_stage = c_stage + 1 == kStages ? 0 : c_stage + 1;
-    ci += n;
-    for (int i = 0; i < n && ci < ntiles; ++i) walk_next(cw, a, lane);
+    if (lane == 0) mbar_arrive(fb + 8);
+    cs = cs + 1 == kStages ? 0 : cs + 1;
+    if (last) break;
   }
-
-  if (!aborted) {
-    finalize(c_seg);
-  } else {
-    // a wait expired: flag it and drain this warp's own copies (bounded) so no
-    // bulk copy still targets shared memory when the warp stops
+  if (aborted) {
     if (lane == 0) flag(a.status, TQ_DEV_TIMEOUT);
-    for (int s = 0; s < kStages; ++s)
-      if ((stage_busy >> s) & 1u) mbar_wait(bars + 8 * s, (c_phase >> s) & 1u);
-    for (int qs = 0; qs < 2; ++qs)
-      if ((q_pending >> qs) & 1u) mbar_wait(bars + 8 * (kStages + qs), (q_phase >> qs) & 1u);
+  } else if (c_seg >= 0) {
+    finalize(c_seg);
   }
+}
+
+// ---------------------------------------------------------------- split kernel
+
+// Warp 0 is the producer; warps 1 .. W are consumers. One CTA per SM.
+template <int KMODE, int GBIG, typename TQ>
+__global__ void __launch_bounds__((kMaxConsumers + 1) * 32, 1)
+split_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t s_dyn[];
+  const int warp = threadIdx.x >> 5;
+  const int W = static_cast<int>(blockDim.x >> 5) - 1;
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(s_dyn));
+  const uint32_t end = base + static_cast<uint32_t>(a.dyn_bytes);
+  constexpr uint32_t kLut = lut_bytes<KMODE>();
+  const uint32_t lut = kLut ? lut_at(base, kLut) : end;
+  const uint32_t bars = base;
+  const uint32_t first = base + kBarBytes;
+  const bool fits = W >= 1 && W <= kMaxConsumers && (!kLut || lut + kLut <= end) &&
+                    stage_at(first, lut, kLut, a.stage_bytes, W * kStages - 1) + a.stage_bytes <= end;
+  if (!__syncthreads_and(fits)) {   // launch misconfigured: flag and leave
+    if (threadIdx.x == 0) flag(a.status, TQ_DEV_TIMEOUT);
+    return;
+  }
+  if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2 * W * kStages; ++i) mbar_init(bars + 8 * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();   // LUT built, barriers initialised
+  if (warp == 0) producer_warp(a, W, bars, first, lut, kLut);
+  else consumer_warp<KMODE, GBIG, TQ>(a, W, warp - 1, bars, first, lut, kLut);
 }
 
 // ---------------------------------------------------------------- reduce
@@ -941,25 +937,23 @@ tq_status make_plan(const tq_config* cfg, int batch, int max_seq_len, int bt_str
 }
 
 struct LaunchShape {
-  int warps;        // per CTA
-  int warp_bytes;
+  int consumers;    // consumer warps per CTA (one producer warp besides)
   int stage_bytes;
+  int q_off, desc_off;
   int dyn_bytes;
 };
 
-// Warps whose buffers fit around a LUT aligned to its size, for a dynamic
-// shared-memory window starting at `start` (the plan the kernel computes).
-int warps_that_fit(uint32_t start, uint32_t dyn, uint32_t lut, uint32_t wb) {
-  const uint32_t lut_at = lut ? ((start + lut - 1) & ~(lut - 1)) : start + dyn;
-  if (lut && lut_at + lut > start + dyn) return 0;
-  int n = 0;
-  uint32_t p = start;
-  for (;;) {
-    if (lut && p < lut_at + lut && p + wb > lut_at) p = lut_at + lut;
-    if (p + wb > start + dyn) return n;
-    p += wb;
-    ++n;
-  }
+// Consumer warps whose rings fit around the barrier block and the LUT in a
+// dynamic shared-memory window of `dyn` bytes starting at `start` (the plan
+// the kernel computes); 0 if the LUT itself does not fit.
+int consumers_that_fit(uint32_t start, uint32_t dyn, uint32_t klut, uint32_t sb) {
+  const uint32_t end = start + dyn;
+  const uint32_t lut = klut ? lut_at(start, klut) : end;
+  if (klut && lut + klut > end) return 0;
+  const uint32_t first = start + kBarBytes;
+  int w = kMaxConsumers;
+  while (w > 0 && stage_at(first, lut, klut, sb, w * kStages - 1) + sb > end) --w;
+  return w;
 }
 
 template <int KMODE>
@@ -967,17 +961,16 @@ bool launch_shape(int tile_bytes, int group, LaunchShape* s) {
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
-  s->stage_bytes = kChunk * tile_bytes;
-  s->warp_bytes = kStages * s->stage_bytes + 2 * group * kD * 2 + 8 * (kStages + 2);
-  s->warp_bytes = (s->warp_bytes + 15) & ~15;
-  const uint32_t lut = lut_bytes<KMODE>();
+  s->q_off = kChunk * tile_bytes;
+  s->desc_off = s->q_off + group * kD * 2;
+  s->stage_bytes = (s->desc_off + 16 + 127) & ~127;
+  const uint32_t klut = lut_bytes<KMODE>();
   // the window may start at 0 or after a small reserved area; take the worse
-  int warps = warps_that_fit(0, optin, lut, s->warp_bytes);
-  const int w2 = warps_that_fit(1024, optin, lut, s->warp_bytes);
-  if (w2 < warps) warps = w2;
-  if (warps > kMaxWarps) warps = kMaxWarps;
-  if (warps < 1) return false;
-  s->warps = warps;
+  int w = consumers_that_fit(0, optin, klut, s->stage_bytes);
+  const int w2 = consumers_that_fit(1024, optin, klut, s->stage_bytes);
+  if (w2 < w) w = w2;
+  if (w < 1) return false;
+  s->consumers = w;
   s->dyn_bytes = optin;
   return true;
 }
@@ -987,13 +980,14 @@ cudaError_t launch_split_typed(DecodeArgs a, cudaStream_t s, int sms) {
   LaunchShape sh;
   if (!launch_shape<KMODE>(a.tile_bytes, a.group, &sh)) return cudaErrorInvalidConfiguration;
   a.stage_bytes = sh.stage_bytes;
-  a.warp_bytes = sh.warp_bytes;
+  a.q_off = sh.q_off;
+  a.desc_off = sh.desc_off;
   a.dyn_bytes = sh.dyn_bytes;
   a.qbuf_bytes = a.group * kD * 2;
   auto k = split_kernel<KMODE, GBIG, TQ>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, a.dyn_bytes);
   if (err != cudaSuccess) return err;
-  k<<<static_cast<unsigned>(sms), sh.warps * 32, static_cast<size_t>(a.dyn_bytes), s>>>(a);
+  k<<<static_cast<unsigned>(sms), (sh.consumers + 1) * 32, static_cast<size_t>(a.dyn_bytes), s>>>(a);
   return cudaGetLastError();
 }
 
@@ -1006,13 +1000,14 @@ cudaError_t launch_split(const DecodeArgs& a, int q_dtype, cudaStream_t s, int s
                      : launch_split_typed<KMODE, 0, __half>(a, s, sms);
 }
 
+// Consumer warps per CTA of the split launch (the reduce needs the count).
 int split_warps_per_cta(const tq_layout& L, int group) {
   LaunchShape sh;
   bool ok;
   if (L.key_fp8) ok = launch_shape<kFp8>(L.tile_bytes, group, &sh);
   else if (L.key_bits == 4) ok = launch_shape<kMse4>(L.tile_bytes, group, &sh);
   else ok = launch_shape<kMse3>(L.tile_bytes, group, &sh);
-  return ok ? sh.warps : 0;
+  return ok ? sh.consumers : 0;
 }
 
 tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* q, int q_dtype,
@@ -1062,13 +1057,14 @@ tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* 
   a.cap = P.cap;
   a.tile_bytes = P.L.tile_bytes;
   a.stage_bytes = 0;
+  a.q_off = 0;
+  a.desc_off = 0;
   a.k_off = P.L.k_off;
   a.v_off = P.L.v_off;
   a.knorm_off = P.L.knorm_off;
   a.vscale_off = P.L.vscale_off;
   a.vzero_off = P.L.vzero_off;
   a.qbuf_bytes = 0;
-  a.warp_bytes = 0;
   a.dyn_bytes = 0;
   const float sm_scale = scale > 0.f ? scale : 0.088388347648318440f;   // 1/sqrt(128)
   a.qscale = sm_scale * 1.4426950408889634f;                              // log2(e)

@@ -15,7 +15,7 @@
 //
 //  Work split. The cache positions are cut into 16-token tiles; the tiles of
 //  all (sequence, KV head) pairs, in (b, h, t) order, form one line of T tiles
-//  that is cut into equal contiguous ranges, one per warp of a persistent grid
+//  that is cut into equal contiguous ranges, one per consumer warp of a persistent grid
 //  (stream-K). A warp's range crosses (b, h) "segments" (optionally also cut at
 //  every partition_tokens positions); for every segment it touches the warp
 //  writes one partial record (acc / l, lse for all G query heads) at index
@@ -838,18 +838,28 @@ __device__ __forceinline__ int reduce_len(const ReduceArgs& a, int b) {
   return min(max(__ldg(a.seq_lens + b), 0), min(a.max_seq_len, a.cap));
 }
 
-// One CTA per (query head, sequence): merge the records of every
-// (segment, warp) piece of this sequence's KV head.
+// One CTA per (query head, sequence), thread d = coordinate. The records of a
+// segment are those of the consumer warps whose ranges overlap it, a
+// contiguous warp range; every thread walks that range 16 warps at a time,
+// loads the LSEs and its partial coordinates of all of them at once (record 0
+// stands in for a warp whose range is empty, and a select, not a multiply,
+// drops it: the workspace may hold any bits), and merges them online.
+constexpr int kReduceChunk = 16;
+
 template <typename TO>
 __global__ void __launch_bounds__(kD) reduce_kernel(const ReduceArgs a) {
   __shared__ long long s_pre[2];
-  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  const int h = hq / a.group, gg = hq - h * a.group;
-  if (threadIdx.x < 32) {   // tiles before sequence b, and in total
+  __shared__ int s_len;
+  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31;
+  const int G = a.group;
+  const int h = hq / G, gg = hq - h * G;
+  if (d < 32) {   // tiles before sequence b, and in total; the length of b
     long long before = 0, total = 0;
     for (int b0 = 0; b0 < a.batch; b0 += 32) {
-      const int j = b0 + threadIdx.x;
-      long long nt = j < a.batch ? (reduce_len(a, j) + kTileTokens - 1) / kTileTokens : 0;
+      const int j = b0 + lane;
+      const int len_j = j < a.batch ? reduce_len(a, j) : 0;
+      if (j == b) s_len = len_j;
+      long long nt = (len_j + kTileTokens - 1) / kTileTokens;
       long long nb = j < b ? nt : 0;
       for (int o = 1; o < 32; o <<= 1) {
         nt += __shfl_xor_sync(0xffffffffu, nt, o);
@@ -858,38 +868,57 @@ __global__ void __launch_bounds__(kD) reduce_kernel(const ReduceArgs a) {
       total += nt;
       before += nb;
     }
-    if (threadIdx.x == 0) { s_pre[0] = before * a.n_kv; s_pre[1] = total * a.n_kv; }
+    if (d == 0) { s_pre[0] = before * a.n_kv; s_pre[1] = total * a.n_kv; }
   }
   __syncthreads();
   const long long orow = static_cast<long long>(b) * a.n_q + hq;
-  const int len = reduce_len(a, b);
+  const int len = s_len;
   if (len <= 0) { store_out<TO>(a.out, orow * kD + d, 0.f); return; }
   const int nt = (len + kTileTokens - 1) / kTileTokens;
   const long long T = s_pre[1], nw = a.num_warps;
+  const long long Tq = T / nw, Tr = T - Tq * nw;   // warp w owns tiles [T w / nw, T (w + 1) / nw)
   const long long seq0 = s_pre[0] + static_cast<long long>(h) * nt;   // first tile of (b, h)
   const int ppt = a.part_tiles > 0 ? a.part_tiles : nt;
   const int parts = (nt + ppt - 1) / ppt;
-  float mx = -INFINITY, acc = 0.f, den = 0.f;
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int p = 0; p < parts; ++p) {
-      const long long t0 = seq0 + static_cast<long long>(p) * ppt;
-      const long long t1 = seq0 + min(static_cast<long long>(p + 1) * ppt, static_cast<long long>(nt));
-      const long long seg = (static_cast<long long>(b) * a.n_kv + h) * a.num_parts + p;
-      const long long wf = ((t0 + 1) * nw - 1) / T, wl = (t1 * nw - 1) / T;
-      for (long long w = wf; w <= wl; ++w) {
-        if (T * w / nw == T * (w + 1) / nw) continue;   // this warp owns no tile
-        const long long rec = (seg + w) * a.group + gg;
-        const float lse = a.rec_lse[rec];
-        if (pass == 0) {
-          mx = fmaxf(mx, lse);
-        } else if (lse != -INFINITY) {
-          const float wgt = exp2f(lse - mx);
-          den += wgt;
-          acc = fmaf(wgt, a.rec_o[rec * kD + d], acc);
+  float acc = 0.f, den = 0.f, mx = -INFINITY;
+  for (int p = 0; p < parts; ++p) {
+    const long long t0 = seq0 + static_cast<long long>(p) * ppt;
+    const long long t1 = seq0 + min(static_cast<long long>(p + 1) * ppt, static_cast<long long>(nt));
+    const long long seg = (static_cast<long long>(b) * a.n_kv + h) * a.num_parts + p;
+    const long long wf = ((t0 + 1) * nw - 1) / T, wl = (t1 * nw - 1) / T;
+    for (long long wb = wf; wb <= wl; wb += kReduceChunk) {
+      const int cnt = static_cast<int>(min(static_cast<long long>(kReduceChunk), wl - wb + 1));
+      long long q = T * wb / nw, r = T * wb - q * nw;   // first tile of warp wb, and remainder
+      float lse[kReduceChunk], x[kReduceChunk];
+#pragma unroll
+      for (int i = 0; i < kReduceChunk; ++i) {
+        lse[i] = -INFINITY;
+        x[i] = 0.f;
+        if (i < cnt) {
+          long long nq = q + Tq, nr = r + Tr;
+          if (nr >= nw) { nr -= nw; ++nq; }
+          const bool ok = nq != q;   // warp wb + i owns at least one tile
+          q = nq;
+          r = nr;
+          const long long rec = ok ? seg + wb + i : 0;
+          if (ok) lse[i] = a.rec_lse[rec * G + gg];
+          x[i] = a.rec_o[(rec * G + gg) * kD + d];
         }
       }
+      float nm = mx;
+#pragma unroll
+      for (int i = 0; i < kReduceChunk; ++i) nm = fmaxf(nm, lse[i]);
+      const float al = mx == -INFINITY ? 0.f : exp2f(mx - nm);
+      acc *= al;
+      den *= al;
+#pragma unroll
+      for (int i = 0; i < kReduceChunk; ++i) {
+        const float w = lse[i] == -INFINITY ? 0.f : exp2f(lse[i] - nm);
+        den += w;
+        acc = w != 0.f ? fmaf(w, x[i], acc) : acc;
+      }
+      mx = nm;
     }
-    if (pass == 0 && mx == -INFINITY) break;
   }
   store_out<TO>(a.out, orow * kD + d, den > 0.f ? acc / den : 0.f);
 }

@@ -22,27 +22,35 @@
 //  segment + warp, which is unique because both sequences are monotone. Every
 //  warp does the same amount of work whatever the sequence lengths are.
 //
-//  Data movement. One CTA per SM: a producer warp and up to 10 consumer
-//  warps. Producer lane j walks consumer j's range chunk by chunk (a chunk is
-//  up to 2 consecutive tiles of one segment), reads block ids one chunk ahead,
-//  and fills consumer j's ring of 3 stages: a 16-byte descriptor (segment,
-//  first position, length, tile count, valid mask, last/new-segment bits), the
-//  tiles by cp.async.bulk (one 2144-byte copy per tile at 4bit_nc) and the
-//  segment's query rows when the chunk opens a segment, all completing on the
-//  stage's "full" mbarrier. Consumers only read descriptors and compute, and
-//  release a stage through its "empty" mbarrier. Every wait is bounded: a
-//  consumer whose wait expires flags TQ_DEV_TIMEOUT and stops; the producer
-//  gives up after a long stretch without progress and, in every case, waits
-//  (bounded) for all copies it issued before it leaves.
+//  Data movement. One CTA per SM: a producer warp and up to 11 consumer
+//  warps (3 warps per sub-partition). Producer lane j walks consumer j's range
+//  chunk by chunk (a chunk is up to 2 consecutive tiles of one segment), loads
+//  the next chunk's block ids while the current one is issued (read one pass
+//  later, so the load latency overlaps other lanes' work), and fills consumer
+//  j's ring of 3 stages: a 16-byte descriptor (segment, first position,
+//  length, tile count, valid mask, last/new-segment bits) and the tiles by
+//  cp.async.bulk (one 2144-byte copy per tile at 4bit_nc), completing on the
+//  stage's "full" mbarrier. A chunk that opens a segment also brings the
+//  segment's query rows into the consumer's query slot, once the consumer has
+//  taken the previous rows ("q empty" mbarrier). Consumers only read
+//  descriptors and compute, and release a stage through its "empty" mbarrier.
+//  The producer starts as soon as the barriers exist; the consumers build the
+//  LUT meanwhile. Every wait is bounded: a consumer whose wait expires flags
+//  TQ_DEV_TIMEOUT and stops; the producer gives up after a long stretch
+//  without progress and, in every case, waits (bounded) for all copies it
+//  issued before it leaves.
 //
 //  Math. Both contractions run on tensor cores with mma.sync.m16n8k16 (f16 in,
 //  f32 accumulate; one such mma occupies a sub-partition's tensor pipe for
 //  about 8 cycles on GB300, so the layout wastes as few rows as possible):
 //    S[8 tok x 2 parts, 8] = K . Q^T. Rows g and 8 + g hold token g with the
 //      centroid hi and lo parts (c = c_hi + c_lo in fp16); one 8-byte LUT entry
-//      per key byte (32 copies, one per lane, so lookups never conflict; the
-//      table is aligned so one PRMT forms the address) is exactly the (row g,
+//      per key byte (16 copies, one per lane of a half warp, so lookups never
+//      conflict; the table is aligned so one PRMT forms the address) is exactly
+//      the (row g,
 //      row 8 + g) operand pair, and the two rows are summed in the same lane.
+//      The 2 tiles of a chunk run in lock step, so 4 accumulation chains
+//      interleave.
 //      Columns 0..3 hold q_hi of the G <= 4 query heads and columns 4..7 q_lo of
 //      the same heads (q = q_hi + q_lo), so one mma per 16 coordinates covers
 //      all products to ~2^-22 relative (fp16 operands alone miss the 2e-3
@@ -71,6 +79,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <climits>
 #include <type_traits>
 
 #include "tq_internal.h"
@@ -80,22 +89,37 @@ namespace {
 
 constexpr int kD = 128;
 #ifndef TQ_DECODE_WARPS
-#define TQ_DECODE_WARPS 10
+#define TQ_DECODE_WARPS 11
 #endif
 constexpr int kMaxConsumers = TQ_DECODE_WARPS;   // consumer warps per CTA (fewer when shared memory is short)
-constexpr int kChunk = 2;               // tiles per ring stage (32 positions)
-constexpr int kStages = 3;              // ring stages per consumer warp
-constexpr uint32_t kBarBytes = 512;     // mbarrier block at the start of shared memory
+#ifndef TQ_DECODE_CHUNK
+#define TQ_DECODE_CHUNK 2
+#endif
+#ifndef TQ_DECODE_STAGES
+#define TQ_DECODE_STAGES 3
+#endif
+#ifndef TQ_PRODUCER_SLEEP_NS
+#define TQ_PRODUCER_SLEEP_NS 64
+#endif
+constexpr int kChunk = TQ_DECODE_CHUNK;     // tiles per ring stage
+constexpr int kStages = TQ_DECODE_STAGES;   // ring stages per consumer warp
 constexpr float kTau = 8.0f;            // lazy rescale threshold, log2 units
 constexpr uint32_t kWaitLimit = 1u << 16;
-constexpr uint32_t kSuspendNs = 20000;  // try_wait suspend hint: bound ~ kWaitLimit * 20 us
+#ifndef TQ_SUSPEND_NS
+#define TQ_SUSPEND_NS 20000
+#endif
+constexpr uint32_t kSuspendNs = TQ_SUSPEND_NS;  // try_wait suspend hint: bound ~ kWaitLimit * hint
 constexpr int kProducerSpin = 1 << 21;  // producer polls without progress before it gives up
 constexpr int kMaxCtas = 256;           // grid cap; sizes the workspace without a device query
 constexpr int kRecordWarps = 16;        // consumer warps per CTA the workspace allows for
 static_assert(kMaxConsumers <= kRecordWarps, "workspace sized for at most 16 consumer warps per CTA");
 static_assert(kMaxConsumers <= 32, "one producer lane per consumer warp");
-static_assert(2 * kMaxConsumers * kStages * 8 <= static_cast<int>(kBarBytes), "barrier block too small");
-static_assert(kStages >= 2 && kStages <= 3, "consumer stage select handles 2 or 3 stages");
+// Shared-memory head: mbarriers (full and empty per (consumer, stage), then one
+// "q empty" per consumer) in the first kBarHead bytes, then one query slot of
+// G * d * 2 bytes per consumer.
+constexpr uint32_t kBarHead = 1024;
+static_assert((2 * kMaxConsumers * kStages + kMaxConsumers) * 8 <= static_cast<int>(kBarHead), "barrier area");
+static_assert(kStages >= 2 && kChunk >= 1 && kChunk <= 4, "ring shape");
 
 enum KeyMode { kMse4 = 4, kMse3 = 3, kFp8 = 8 };
 
@@ -114,8 +138,8 @@ struct DecodeArgs {
   int num_parts;       // partitions per (b, h) in the record index
   int max_seq_len, cap;
   int tile_bytes, k_off, v_off, knorm_off, vscale_off, vzero_off;
-  int stage_bytes;     // ring stage: kChunk tiles, query rows, descriptor
-  int q_off, desc_off; // offsets of the query rows and the descriptor in a stage
+  int stage_bytes;     // ring stage: kChunk tiles, then the descriptor
+  int desc_off;        // offset of the descriptor in a stage
   int qbuf_bytes;      // G * d * 2
   int dyn_bytes;
   float qscale;        // softmax scale * log2(e)
@@ -270,24 +294,26 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 
 // ---------------------------------------------------------------- LUT
 
-// Entry e (a key byte, or a 6-bit pair of 3-bit indices) holds, for each of 32
-// lanes, uint2 {half2(c_hi[lo idx], c_hi[hi idx]), half2(c_lo[..], c_lo[..])};
-// entry stride 256 bytes. The table is aligned to its own size, so the address
-// of (entry, lane) is the entry number OR-ed into bits 8.. of the lane's base:
-// for 4-bit keys a single byte permute of the key word.
+// Entry e (a key byte, or a 6-bit pair of 3-bit indices) holds 16 copies of
+// uint2 {half2(c_hi[lo idx], c_hi[hi idx]), half2(c_lo[..], c_lo[..])}, one per
+// lane of a half warp (an 8-byte shared load is served per half warp, so lanes
+// l and l + 16 sharing a copy never conflict); entry stride 256 bytes. The
+// table is aligned to its own size, so the address of (entry, lane) is the
+// entry number OR-ed into bits 8.. of the lane's base: for 4-bit keys a single
+// byte permute of the key word.
 template <int KMODE>
 __host__ __device__ constexpr uint32_t lut_bytes() { return KMODE == kMse4 ? 65536u : (KMODE == kMse3 ? 16384u : 0u); }
 
 template <int KMODE>
-__device__ void build_lut(uint32_t lut, const float* cent) {
+__device__ void build_lut(uint32_t lut, const float* cent, int tid, int nthreads) {
   constexpr int kEntries = KMODE == kMse4 ? 256 : 64;
   constexpr int kShift = KMODE == kMse4 ? 4 : 3;
   constexpr int kMask = (1 << kShift) - 1;
-  for (int i = threadIdx.x; i < kEntries * 32; i += blockDim.x) {
-    const int e = i >> 5;
+  for (int i = tid; i < kEntries * 16; i += nthreads) {
+    const int e = i >> 4;
     uint32_t hi, lo;
     split_half2(cent[e & kMask], cent[(e >> kShift) & kMask], hi, lo);
-    sts64(lut + 8u * i, make_uint2(hi, lo));
+    sts64(lut + 256u * e + 8u * (i & 15), make_uint2(hi, lo));
   }
 }
 
@@ -321,8 +347,8 @@ __host__ __device__ __forceinline__ uint32_t stage_at(uint32_t first, uint32_t l
   return first + static_cast<uint32_t>(idx) * sb;
 }
 
-__host__ __device__ __forceinline__ uint32_t lut_at(uint32_t base, uint32_t klut) {
-  return (base + kBarBytes + klut - 1) & ~(klut - 1);
+__host__ __device__ __forceinline__ uint32_t lut_at(uint32_t base, uint32_t klut, uint32_t head) {
+  return (base + head + klut - 1) & ~(klut - 1);
 }
 
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
@@ -347,19 +373,43 @@ __device__ __forceinline__ int clamp_len(const DecodeArgs& a, int len) {
 __device__ __forceinline__ uint32_t full_bar(uint32_t bars, int j, int s) {
   return bars + 16u * static_cast<uint32_t>(j * kStages + s);
 }
+// Consumer j has taken the query rows of its latest segment.
+__device__ __forceinline__ uint32_t q_empty_bar(uint32_t bars, int W, int j) {
+  return bars + 8u * static_cast<uint32_t>(2 * W * kStages + j);
+}
 
 // ---------------------------------------------------------------- producer warp
 
+// Position in the (b, h, t) tile line of one producer lane.
+struct Cursor {
+  int b, h, t, nt, len;
+};
+
+// Next tile; skips empty sequences. Call only while tiles remain after this one.
+__device__ __forceinline__ void cursor_next(Cursor& u, const DecodeArgs& a) {
+  if (++u.t < u.nt) return;
+  u.t = 0;
+  if (++u.h < a.n_kv) return;
+  u.h = 0;
+  do {
+    ++u.b;
+    u.len = clamp_len(a, __ldg(a.seq_lens + u.b));
+    u.nt = (u.len + kTileTokens - 1) / kTileTokens;
+  } while (u.nt == 0);
+}
+
 // Lane j < W feeds consumer warp j of this CTA: it walks that warp's range of
 // the tile line chunk by chunk (a chunk is up to kChunk consecutive tiles of
-// one segment), reads the chunk's block ids one chunk ahead, and for each
-// chunk fills the next free ring stage: a 16-byte descriptor
-// {segment, first position, sequence length, n | valid mask << 4 | last << 8 |
-// new segment << 9}, the tiles by cp.async.bulk, and the segment's query rows
-// when the chunk opens a segment. A consumer whose range is empty gets one
-// descriptor with n = 0 and the last bit.
-__device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_t first, uint32_t lut,
-                              uint32_t klut) {
+// one segment) and, for each chunk, fills the next free ring stage with a
+// 16-byte descriptor {segment, first position, sequence length, n | valid mask
+// << 4 | last << 8 | new segment << 9} and the tiles (cp.async.bulk). A chunk
+// that opens a segment also brings the segment's query rows into the
+// consumer's query slot, once the consumer has taken the previous rows (its
+// "q empty" barrier). A consumer whose range is empty gets one descriptor with
+// n = 0 and the last bit. The block ids of the next chunk are loaded when the
+// current one is issued, so their latency overlaps the wait for a free stage.
+__device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_t qslots, uint32_t first,
+                              uint32_t lut, uint32_t klut) {
   const int lane = threadIdx.x & 31;
   const bool mine = lane < W;
   const long long nw = static_cast<long long>(gridDim.x) * W;
@@ -368,13 +418,16 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
   // tiles of the whole line: n_kv * sum_b ceil(len_b / 16)
   long long total = 0;
   bool too_long = false;
+  int len0 = 0;   // clamped length of sequence `lane` (first group)
   for (int b0 = 0; b0 < a.batch; b0 += 32) {
     const int j = b0 + lane;
     int nt = 0;
     if (j < a.batch) {
       const int raw = __ldg(a.seq_lens + j);
       too_long |= raw > min(a.max_seq_len, a.cap);
-      nt = (clamp_len(a, raw) + kTileTokens - 1) / kTileTokens;
+      const int len = clamp_len(a, raw);
+      if (b0 == 0) len0 = len;
+      nt = (len + kTileTokens - 1) / kTileTokens;
     }
     for (int o_ = 1; o_ < 32; o_ <<= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o_);
     total += nt;
@@ -382,17 +435,17 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
   if (blockIdx.x == 0 && __any_sync(0xffffffffu, too_long) && lane == 0) flag(a.status, TQ_DEV_SEQ_TOO_LONG);
   total *= a.n_kv;
   const long long r0 = mine ? total * wid / nw : 0;
-  long long rem = mine ? total * (wid + 1) / nw - r0 : 0;
+  long long rem = mine ? total * (wid + 1) / nw - r0 : 0;   // tiles left to plan
 
-  // cursor: first tile of this lane's range, found for all lanes together over
-  // groups of 32 sequences
-  int cb = 0, ch = 0, ct = 0, cnt = 0, clen = 0;
+  // locate r0: per group of 32 sequences an inclusive scan of their tile
+  // counts, then a per-lane binary search over it
+  Cursor pc = {0, 0, 0, 0, 0};
   {
     bool found = rem <= 0;
     long long acc = 0;   // tiles before the group
     for (int b0 = 0; b0 < a.batch && __any_sync(0xffffffffu, !found); b0 += 32) {
       const int bb = b0 + lane;
-      const int len = bb < a.batch ? clamp_len(a, __ldg(a.seq_lens + bb)) : 0;
+      const int len = bb < a.batch ? (b0 == 0 ? len0 : clamp_len(a, __ldg(a.seq_lens + bb))) : 0;
       const int nt = (len + kTileTokens - 1) / kTileTokens;
       const long long span = static_cast<long long>(nt) * a.n_kv;
       long long inc = span;
@@ -400,27 +453,32 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
         const long long y = __shfl_up_sync(0xffffffffu, inc, o_);
         if (lane >= o_) inc += y;
       }
-      const long long excl = acc + inc - span;
-      for (int k = 0; k < W; ++k) {
-        if (!__shfl_sync(0xffffffffu, static_cast<int>(!found), k)) continue;
-        const long long x = __shfl_sync(0xffffffffu, r0, k);
-        const int idx = __popc(__ballot_sync(0xffffffffu, bb < a.batch && excl + span <= x));
-        if (idx < 32 && b0 + idx < a.batch) {
-          const long long e = __shfl_sync(0xffffffffu, excl, idx & 31);
-          const int n_t = __shfl_sync(0xffffffffu, nt, idx & 31);
-          const int ln = __shfl_sync(0xffffffffu, len, idx & 31);
-          if (lane == k) {
-            found = true;
-            cb = b0 + idx;
-            const int off = static_cast<int>(x - e);
-            ch = off / n_t;
-            ct = off - ch * n_t;
-            cnt = n_t;
-            clen = ln;
-          }
-        }
+      const long long gtotal = __shfl_sync(0xffffffffu, inc, 31);
+      const long long key = bb < a.batch ? acc + inc : LLONG_MAX;   // end of sequence bb's tiles
+      // idx = number of sequences of the group that end at or before r0
+      int idx = 0;
+#pragma unroll
+      for (int step = 16; step >= 1; step >>= 1) {
+        const long long v = __shfl_sync(0xffffffffu, key, idx + step - 1);
+        if (v <= r0) idx += step;
       }
-      acc += __shfl_sync(0xffffffffu, inc, 31);
+      const long long k31 = __shfl_sync(0xffffffffu, key, 31);
+      if (idx == 31 && k31 <= r0) idx = 32;
+      const int src = idx & 31;
+      const long long e_end = __shfl_sync(0xffffffffu, key, src);
+      const long long e_span = __shfl_sync(0xffffffffu, span, src);
+      const int n_t = __shfl_sync(0xffffffffu, nt, src);
+      const int ln = __shfl_sync(0xffffffffu, len, src);
+      if (!found && idx < 32 && b0 + idx < a.batch) {
+        found = true;
+        const int off = static_cast<int>(r0 - (e_end - e_span));
+        pc.b = b0 + idx;
+        pc.h = off / n_t;
+        pc.t = off - pc.h * n_t;
+        pc.nt = n_t;
+        pc.len = ln;
+      }
+      acc += gtotal;
     }
   }
 
@@ -430,84 +488,85 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
 #pragma unroll
   for (int i = 0; i < kChunk; ++i) n_blk[i] = -1;
   auto plan = [&]() {
-    int n = min(kChunk, cnt - ct);
+    int n = min(kChunk, pc.nt - pc.t);
     if (rem < n) n = static_cast<int>(rem);
-    if (a.part_tiles > 0) n = min(n, a.part_tiles - ct % a.part_tiles);
+    if (a.part_tiles > 0) n = min(n, a.part_tiles - pc.t % a.part_tiles);
     n_n = n;
-    n_b = cb;
-    n_h = ch;
-    n_t = ct;
-    n_len = clen;
-    n_seg = (cb * a.n_kv + ch) * a.num_parts + (a.part_tiles > 0 ? ct / a.part_tiles : 0);
-    const int* row = a.block_table + static_cast<long long>(cb) * a.bt_stride;
+    n_b = pc.b;
+    n_h = pc.h;
+    n_t = pc.t;
+    n_len = pc.len;
+    n_seg = (pc.b * a.n_kv + pc.h) * a.num_parts + (a.part_tiles > 0 ? pc.t / a.part_tiles : 0);
+    const int* row = a.block_table + static_cast<long long>(pc.b) * a.bt_stride;
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) n_blk[i] = i < n ? __ldg(row + (((ct + i) << 4) >> a.log2_bs)) : -1;
+    for (int i = 0; i < kChunk; ++i) n_blk[i] = i < n ? __ldg(row + (((pc.t + i) << 4) >> a.log2_bs)) : -1;
     rem -= n;
-    ct += n;
-    if (ct == cnt && rem > 0) {   // next (sequence, head); skip empty sequences
-      ct = 0;
-      if (++ch == a.n_kv) {
-        ch = 0;
-        do {
-          ++cb;
-          clen = clamp_len(a, __ldg(a.seq_lens + cb));
-          cnt = (clen + kTileTokens - 1) / kTileTokens;
-        } while (cnt == 0);
-      }
-    }
+    for (int i = 0; i < n && rem > 0; ++i) cursor_next(pc, a);
   };
   if (mine && rem > 0) plan();
 
   const uint64_t policy = evict_first_policy();
+  const uint32_t qslot = qslots + static_cast<uint32_t>(mine ? lane : 0) * a.qbuf_bytes;
+  const uint32_t qbar = q_empty_bar(bars, W, mine ? lane : 0);
   uint32_t eparity = (1u << kStages) - 1;   // empty-barrier parity to wait for, per stage
   uint32_t used = 0, fpar = 0;              // stages ever filled; parity of their next fill
   int ps = 0, prev_seg = -1;
+  int qn = 0, qdone = 0;                    // query copies issued / known consumed
   bool done = !mine;
   int idle = 0;
   while (__any_sync(0xffffffffu, !done)) {
     bool progressed = false;
-    if (!done) {
-      const uint32_t fb = full_bar(bars, lane, ps);
-      if (mbar_test(fb + 8, (eparity >> ps) & 1u)) {
-        eparity ^= 1u << ps;
-        const uint32_t sa = stage_at(first, lut, klut, a.stage_bytes, lane * kStages + ps);
-        const bool last = rem <= 0;
-        const bool newq = n_n > 0 && n_seg != prev_seg;
-        uint32_t okm = 0, bytes = 0;
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i)
-          if (i < n_n && n_blk[i] >= 0 && n_blk[i] < a.num_blocks) {
-            okm |= 1u << i;
-            bytes += a.tile_bytes;
-          }
-        if (newq) bytes += a.qbuf_bytes;
-        sts128(sa + a.desc_off, make_uint4(static_cast<uint32_t>(n_seg), static_cast<uint32_t>(n_t << 4),
-                                           static_cast<uint32_t>(n_len),
-                                           static_cast<uint32_t>(n_n) | (okm << 4) | (last ? 256u : 0u) |
-                                               (newq ? 512u : 0u)));
-        fence_proxy_async();
-        mbar_expect(fb, bytes);
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i)
-          if ((okm >> i) & 1u) {
-            const uint8_t* src = a.cache + ((static_cast<long long>(n_blk[i]) * a.n_kv + n_h) * a.tiles_per_block +
-                                            ((n_t + i) & (a.tiles_per_block - 1))) *
-                                               static_cast<long long>(a.tile_bytes);
-            bulk_g2s(sa + i * a.tile_bytes, src, a.tile_bytes, fb, policy);
-          }
-        if (newq) {
-          const uint8_t* src = static_cast<const uint8_t*>(a.q) +
-                               (static_cast<long long>(n_b) * a.n_q + n_h * a.group) * (kD * 2);
-          bulk_g2s_plain(sa + a.q_off, src, a.qbuf_bytes, fb);
-        }
-        if (n_n > 0) prev_seg = n_seg;
-        used |= 1u << ps;
-        fpar ^= 1u << ps;
-        ps = ps + 1 == kStages ? 0 : ps + 1;
-        progressed = true;
-        if (last) done = true;
-        else plan();
+#ifndef TQ_PRODUCER_PASSES
+#define TQ_PRODUCER_PASSES 1
+#endif
+    // one chunk per lane per pass: the block ids plan() loads for the next
+    // chunk are only read on the next pass, after other lanes' work
+    for (int pass = 0; pass < TQ_PRODUCER_PASSES && !done; ++pass) {
+      const bool newq = n_n > 0 && n_seg != prev_seg;
+      if (newq && qdone < qn) {   // the slot still holds rows the consumer has not taken
+        if (!mbar_test(qbar, (qn - 1) & 1)) break;
+        qdone = qn;
       }
+      const uint32_t fb = full_bar(bars, lane, ps);
+      if (!mbar_test(fb + 8, (eparity >> ps) & 1u)) break;
+      eparity ^= 1u << ps;
+      const uint32_t sa = stage_at(first, lut, klut, a.stage_bytes, lane * kStages + ps);
+      const bool last = rem <= 0;
+      uint32_t okm = 0, bytes = 0;
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i)
+        if (i < n_n && n_blk[i] >= 0 && n_blk[i] < a.num_blocks) {
+          okm |= 1u << i;
+          bytes += a.tile_bytes;
+        }
+      if (newq) bytes += a.qbuf_bytes;
+      sts128(sa + a.desc_off, make_uint4(static_cast<uint32_t>(n_seg), static_cast<uint32_t>(n_t << 4),
+                                         static_cast<uint32_t>(n_len),
+                                         static_cast<uint32_t>(n_n) | (okm << 4) | (last ? 256u : 0u) |
+                                             (newq ? 512u : 0u)));
+      fence_proxy_async();
+      mbar_expect(fb, bytes);
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i)
+        if ((okm >> i) & 1u) {
+          const uint8_t* src = a.cache + ((static_cast<long long>(n_blk[i]) * a.n_kv + n_h) * a.tiles_per_block +
+                                          ((n_t + i) & (a.tiles_per_block - 1))) *
+                                             static_cast<long long>(a.tile_bytes);
+          bulk_g2s(sa + i * a.tile_bytes, src, a.tile_bytes, fb, policy);
+        }
+      if (newq) {
+        const uint8_t* src = static_cast<const uint8_t*>(a.q) +
+                             (static_cast<long long>(n_b) * a.n_q + n_h * a.group) * (kD * 2);
+        bulk_g2s_plain(qslot, src, a.qbuf_bytes, fb);
+        ++qn;
+      }
+      if (n_n > 0) prev_seg = n_seg;
+      used |= 1u << ps;
+      fpar ^= 1u << ps;
+      ps = ps + 1 == kStages ? 0 : ps + 1;
+      progressed = true;
+      if (last) done = true;
+      else plan();
     }
     if (__any_sync(0xffffffffu, progressed)) {
       idle = 0;
@@ -515,7 +574,7 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
       if (lane == 0) flag(a.status, TQ_DEV_TIMEOUT);
       break;
     } else {
-      __nanosleep(64);
+      if (TQ_PRODUCER_SLEEP_NS > 0) __nanosleep(TQ_PRODUCER_SLEEP_NS);
     }
   }
   // every copy this lane issued has landed before the warp leaves (bounded)
@@ -534,7 +593,8 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
 //   G > 4: column k is head k; the lo parts run in a second mma into the same
 //     accumulators.
 template <int KMODE, int GBIG, typename TQ>
-__device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, uint32_t first, uint32_t lut,
+__device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, uint32_t qslots, uint32_t first,
+                              uint32_t lut,
                               uint32_t klut) {
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;   // mma groupID
@@ -546,7 +606,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
   const bool colv0 = hd0 < G, colv1 = hd0 + 1 < G;
   const bool colmask = GBIG ? G < 8 : G < 4;    // some columns carry no head
   uint32_t lut_lane = 0;
-  if constexpr (KMODE != kFp8) lut_lane = lut + 8u * lane;
+  if constexpr (KMODE != kFp8) lut_lane = lut + 8u * (lane & 15);
   uint32_t stg[kStages];
 #pragma unroll
   for (int s = 0; s < kStages; ++s) stg[s] = stage_at(first, lut, klut, a.stage_bytes, j * kStages + s);
@@ -631,87 +691,113 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
     l0 = l1 = z0 = z1 = 0.f;
   };
 
-  // one 16-token tile at shared address tb; nvalid of its positions are real
-  auto tile = [&](uint32_t tb, int nvalid) {
-    // ---- S = K . Q^T
-    float v[4];   // [0] tok g col 2c, [1] tok g col 2c+1, [2] tok g+8 col 2c, [3] tok g+8 col 2c+1
+  // the kChunk tiles of a stage at shared address st, in lock-step phases so
+  // their accumulation chains interleave; tile i has nv[i] real positions
+  // (tiles past the chunk's end compute on stale bytes and are fully masked)
+  auto chunk = [&](uint32_t st, const int (&nv)[kChunk]) {
+    // ---- S_i = K_i . Q^T
+    float v[kChunk][4];   // [0] tok g col 2c, [1] tok g col 2c+1, [2] tok g+8 col 2c, [3] tok g+8 col 2c+1
     if constexpr (KMODE == kFp8) {
-      float S[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t kt = tb + a.k_off;
-      const uint4 kg0 = lds128(kt + g * 128 + 32 * c), kg1 = lds128(kt + g * 128 + 32 * c + 16);
-      const uint4 kh0 = lds128(kt + (g + 8) * 128 + 32 * c), kh1 = lds128(kt + (g + 8) * 128 + 32 * c + 16);
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3
-        const uint32_t wg = word_of(s < 4 ? kg0 : kg1, s & 3), wh = word_of(s < 4 ? kh0 : kh1, s & 3);
-        const __half2_raw g01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wg & 0xFFFFu), __NV_E4M3);
-        const __half2_raw g23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wg >> 16), __NV_E4M3);
-        const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh & 0xFFFFu), __NV_E4M3);
-        const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh >> 16), __NV_E4M3);
-        const uint32_t a0 = static_cast<uint32_t>(g01.x) | (static_cast<uint32_t>(g01.y) << 16);
-        const uint32_t a1 = static_cast<uint32_t>(h01.x) | (static_cast<uint32_t>(h01.y) << 16);
-        const uint32_t a2 = static_cast<uint32_t>(g23.x) | (static_cast<uint32_t>(g23.y) << 16);
-        const uint32_t a3 = static_cast<uint32_t>(h23.x) | (static_cast<uint32_t>(h23.y) << 16);
-        mma16816(S, a0, a1, a2, a3, qb[2 * s], qb[2 * s + 1]);
-        if (GBIG) mma16816(S, a0, a1, a2, a3, qb[16 + 2 * s], qb[16 + 2 * s + 1]);
+      for (int i = 0; i < kChunk; ++i) v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        const uint32_t kt = st + i * a.tile_bytes + a.k_off;
+        const uint4 kg0 = lds128(kt + g * 128 + 32 * c), kg1 = lds128(kt + g * 128 + 32 * c + 16);
+        const uint4 kh0 = lds128(kt + (g + 8) * 128 + 32 * c), kh1 = lds128(kt + (g + 8) * 128 + 32 * c + 16);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3
+          const uint32_t wg = word_of(s < 4 ? kg0 : kg1, s & 3), wh = word_of(s < 4 ? kh0 : kh1, s & 3);
+          const __half2_raw g01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wg & 0xFFFFu), __NV_E4M3);
+          const __half2_raw g23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wg >> 16), __NV_E4M3);
+          const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh & 0xFFFFu), __NV_E4M3);
+          const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(wh >> 16), __NV_E4M3);
+          const uint32_t a0 = static_cast<uint32_t>(g01.x) | (static_cast<uint32_t>(g01.y) << 16);
+          const uint32_t a1 = static_cast<uint32_t>(h01.x) | (static_cast<uint32_t>(h01.y) << 16);
+          const uint32_t a2 = static_cast<uint32_t>(g23.x) | (static_cast<uint32_t>(g23.y) << 16);
+          const uint32_t a3 = static_cast<uint32_t>(h23.x) | (static_cast<uint32_t>(h23.y) << 16);
+          mma16816(v[i], a0, a1, a2, a3, qb[2 * s], qb[2 * s + 1]);
+          if (GBIG) mma16816(v[i], a0, a1, a2, a3, qb[16 + 2 * s], qb[16 + 2 * s + 1]);
+        }
       }
-      v[0] = S[0]; v[1] = S[1]; v[2] = S[2]; v[3] = S[3];
     } else {
-      const uint32_t kt = tb + a.k_off;
-      uint4 kg, kh;   // this lane's key slice of tokens g and g+8
-      if constexpr (KMODE == kMse4) {
-        kg = lds128(kt + g * 64 + 16 * c);
-        kh = lds128(kt + (g + 8) * 64 + 16 * c);
-      } else {
-        const uint32_t ra = kt + g * 48 + 12 * c, rb = kt + (g + 8) * 48 + 12 * c;
-        kg = make_uint4(lds32(ra), lds32(ra + 4), lds32(ra + 8), 0u);
-        kh = make_uint4(lds32(rb), lds32(rb + 4), lds32(rb + 8), 0u);
+      uint4 kg[kChunk], kh[kChunk];   // this lane's key slices of tokens g and g+8
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        const uint32_t kt = st + i * a.tile_bytes + a.k_off;
+        if constexpr (KMODE == kMse4) {
+          kg[i] = lds128(kt + g * 64 + 16 * c);
+          kh[i] = lds128(kt + (g + 8) * 64 + 16 * c);
+        } else {
+          const uint32_t ra = kt + g * 48 + 12 * c, rb = kt + (g + 8) * 48 + 12 * c;
+          kg[i] = make_uint4(lds32(ra), lds32(ra + 4), lds32(ra + 8), 0u);
+          kh[i] = make_uint4(lds32(rb), lds32(rb + 4), lds32(rb + 8), 0u);
+        }
       }
       // M rows: 8 tokens x {centroid hi part, centroid lo part}; k-step s holds
       // this lane's coordinates 32c + 4s .. +3 (two key bytes = two LUT entries,
       // each entry = the (hi, lo) operand pair of one row pair)
-      float Sg[4] = {0.f, 0.f, 0.f, 0.f}, Sh[4] = {0.f, 0.f, 0.f, 0.f};
+      float Sg[kChunk][4], Sh[kChunk][4];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) Sg[i][k] = Sh[i][k] = 0.f;
 #pragma unroll
       for (int s2 = 0; s2 < 8; ++s2) {
-        const uint2 g0 = lds64(lut_addr<KMODE>(kg, 2 * s2, lut_lane));
-        const uint2 g1 = lds64(lut_addr<KMODE>(kg, 2 * s2 + 1, lut_lane));
-        const uint2 h0 = lds64(lut_addr<KMODE>(kh, 2 * s2, lut_lane));
-        const uint2 h1 = lds64(lut_addr<KMODE>(kh, 2 * s2 + 1, lut_lane));
-        mma16816(Sg, g0.x, g0.y, g1.x, g1.y, qb[2 * s2], qb[2 * s2 + 1]);
-        mma16816(Sh, h0.x, h0.y, h1.x, h1.y, qb[2 * s2], qb[2 * s2 + 1]);
-        if (GBIG) {
-          mma16816(Sg, g0.x, g0.y, g1.x, g1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
-          mma16816(Sh, h0.x, h0.y, h1.x, h1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+          const uint2 g0 = lds64(lut_addr<KMODE>(kg[i], 2 * s2, lut_lane));
+          const uint2 g1 = lds64(lut_addr<KMODE>(kg[i], 2 * s2 + 1, lut_lane));
+          const uint2 h0 = lds64(lut_addr<KMODE>(kh[i], 2 * s2, lut_lane));
+          const uint2 h1 = lds64(lut_addr<KMODE>(kh[i], 2 * s2 + 1, lut_lane));
+          mma16816(Sg[i], g0.x, g0.y, g1.x, g1.y, qb[2 * s2], qb[2 * s2 + 1]);
+          mma16816(Sh[i], h0.x, h0.y, h1.x, h1.y, qb[2 * s2], qb[2 * s2 + 1]);
+          if (GBIG) {
+            mma16816(Sg[i], g0.x, g0.y, g1.x, g1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
+            mma16816(Sh[i], h0.x, h0.y, h1.x, h1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
+          }
         }
       }
       // rows g (hi part) + g + 8 (lo part) of each token: same lane
-      v[0] = Sg[0] + Sg[2];
-      v[1] = Sg[1] + Sg[3];
-      v[2] = Sh[0] + Sh[2];
-      v[3] = Sh[1] + Sh[3];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        v[i][0] = Sg[i][0] + Sg[i][2];
+        v[i][1] = Sg[i][1] + Sg[i][3];
+        v[i][2] = Sh[i][0] + Sh[i][2];
+        v[i][3] = Sh[i][1] + Sh[i][3];
+      }
     }
 
     // ---- scores: q hi + lo columns, norms, masks
-    if (!GBIG) {
+    float svg[kChunk], svh[kChunk], szg[kChunk], szh[kChunk];
+    float cm0 = -INFINITY, cm1 = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], 2);
+    for (int i = 0; i < kChunk; ++i) {
+      const uint32_t tb = st + i * a.tile_bytes;
+      if (!GBIG) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[i][k] += __shfl_xor_sync(0xffffffffu, v[i][k], 2);
+      }
+      if constexpr (KMODE != kFp8) {
+        const float ng = lds_h2f(tb + a.knorm_off + 2 * g), nh = lds_h2f(tb + a.knorm_off + 2 * g + 16);
+        v[i][0] *= ng; v[i][1] *= ng; v[i][2] *= nh; v[i][3] *= nh;
+      }
+      svg[i] = lds_h2f(tb + a.vscale_off + 2 * g);
+      svh[i] = lds_h2f(tb + a.vscale_off + 2 * g + 16);
+      szg[i] = lds_h2f(tb + a.vzero_off + 2 * g);
+      szh[i] = lds_h2f(tb + a.vzero_off + 2 * g + 16);
+      if (nv[i] < kTileTokens) {   // missing, ragged or past the chunk's end
+        if (g >= nv[i]) { v[i][0] = v[i][1] = -INFINITY; svg[i] = 0.f; szg[i] = 0.f; }
+        if (g + 8 >= nv[i]) { v[i][2] = v[i][3] = -INFINITY; svh[i] = 0.f; szh[i] = 0.f; }
+      }
+      if (colmask) {
+        if (!colv0) v[i][0] = v[i][2] = -INFINITY;
+        if (!colv1) v[i][1] = v[i][3] = -INFINITY;
+      }
+      cm0 = fmaxf(cm0, fmaxf(v[i][0], v[i][2]));
+      cm1 = fmaxf(cm1, fmaxf(v[i][1], v[i][3]));
     }
-    if constexpr (KMODE != kFp8) {
-      const float ng = lds_h2f(tb + a.knorm_off + 2 * g), nh = lds_h2f(tb + a.knorm_off + 2 * g + 16);
-      v[0] *= ng; v[1] *= ng; v[2] *= nh; v[3] *= nh;
-    }
-    float svg = lds_h2f(tb + a.vscale_off + 2 * g), svh = lds_h2f(tb + a.vscale_off + 2 * g + 16);
-    float szg = lds_h2f(tb + a.vzero_off + 2 * g), szh = lds_h2f(tb + a.vzero_off + 2 * g + 16);
-    if (nvalid < kTileTokens) {   // missing or ragged tile
-      if (g >= nvalid) { v[0] = v[1] = -INFINITY; svg = 0.f; szg = 0.f; }
-      if (g + 8 >= nvalid) { v[2] = v[3] = -INFINITY; svh = 0.f; szh = 0.f; }
-    }
-    if (colmask) {
-      if (!colv0) v[0] = v[2] = -INFINITY;
-      if (!colv1) v[1] = v[3] = -INFINITY;
-    }
-    const bool need = fmaxf(v[0], v[2]) > m0 + kTau || fmaxf(v[1], v[3]) > m1 + kTau;
-    if (__any_sync(0xffffffffu, need)) {   // rare: move the running max, rescale
-      float cm0 = fmaxf(v[0], v[2]), cm1 = fmaxf(v[1], v[3]);
+    if (__any_sync(0xffffffffu, cm0 > m0 + kTau || cm1 > m1 + kTau)) {   // rare: move the max, rescale
 #pragma unroll
       for (int o_ = 4; o_ < 32; o_ <<= 1) {
         cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, o_));
@@ -729,31 +815,34 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
     }
 
     // ---- probabilities, P^T operands (movmatrix), O^T += V^T . P^T
-    const float p0 = ex2(v[0] - m0), p1 = ex2(v[1] - m1);
-    const float p2 = ex2(v[2] - m0), p3 = ex2(v[3] - m1);
-    l0 += p0 + p2;
-    l1 += p1 + p3;
-    z0 = fmaf(p0, szg, fmaf(p2, szh, z0));
-    z1 = fmaf(p1, szg, fmaf(p3, szh, z1));
-    uint32_t hg, lg, hh, lh;   // hi/lo half2 of (col 2c, col 2c+1) for tokens g and g+8
-    split_half2(p0 * svg, p1 * svg, hg, lg);
-    split_half2(p2 * svh, p3 * svh, hh, lh);
-    const uint32_t b0 = movmatrix_trans(lo_lane ? lg : hg), b1 = movmatrix_trans(lo_lane ? lh : hh);
-    uint32_t b0l = 0u, b1l = 0u;
-    if (GBIG) { b0l = movmatrix_trans(lg); b1l = movmatrix_trans(lh); }
-    const uint32_t vt = tb + a.v_off + 16 * (g ^ (2 * c));
-    const uint4 va = lds128(vt + 128 * c);         // tokens 2c, 2c+1
-    const uint4 vb = lds128(vt + 128 * (c + 4));   // tokens 2c+8, 2c+9
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t wa = word_of(va, k), wb = word_of(vb, k);
-      const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-      mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0, b1);
-      mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0, b1);
-      if (GBIG) {
-        mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0l, b1l);
-        mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0l,
-                 b1l);
+    for (int i = 0; i < kChunk; ++i) {
+      const float p0 = ex2(v[i][0] - m0), p1 = ex2(v[i][1] - m1);
+      const float p2 = ex2(v[i][2] - m0), p3 = ex2(v[i][3] - m1);
+      l0 += p0 + p2;
+      l1 += p1 + p3;
+      z0 = fmaf(p0, szg[i], fmaf(p2, szh[i], z0));
+      z1 = fmaf(p1, szg[i], fmaf(p3, szh[i], z1));
+      uint32_t hg, lg, hh, lh;   // hi/lo half2 of (col 2c, col 2c+1) for tokens g and g+8
+      split_half2(p0 * svg[i], p1 * svg[i], hg, lg);
+      split_half2(p2 * svh[i], p3 * svh[i], hh, lh);
+      const uint32_t b0 = movmatrix_trans(lo_lane ? lg : hg), b1 = movmatrix_trans(lo_lane ? lh : hh);
+      uint32_t b0l = 0u, b1l = 0u;
+      if (GBIG) { b0l = movmatrix_trans(lg); b1l = movmatrix_trans(lh); }
+      const uint32_t vt = st + i * a.tile_bytes + a.v_off + 16 * (g ^ (2 * c));
+      const uint4 va = lds128(vt + 128 * c);         // tokens 2c, 2c+1
+      const uint4 vb = lds128(vt + 128 * (c + 4));   // tokens 2c+8, 2c+9
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t wa = word_of(va, k), wb = word_of(vb, k);
+        const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+        mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0, b1);
+        mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0, b1);
+        if (GBIG) {
+          mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0l, b1l);
+          mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0l,
+                   b1l);
+        }
       }
     }
   };
@@ -764,7 +853,9 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
     const uint32_t fb = full_bar(bars, j, cs);
     if (!mbar_wait(fb, (fpar >> cs) & 1u)) { aborted = true; break; }
     fpar ^= 1u << cs;
-    const uint32_t sa = cs == 0 ? stg[0] : (cs == 1 ? stg[1] : stg[kStages - 1]);
+    uint32_t sa = stg[0];
+#pragma unroll
+    for (int s = 1; s < kStages; ++s) sa = cs == s ? stg[s] : sa;
     const uint4 desc = lds128(sa + a.desc_off);
     const int n = static_cast<int>(desc.w & 7u);
     const uint32_t okm = (desc.w >> 4) & 0xFu;
@@ -773,14 +864,18 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
       const int seg = static_cast<int>(desc.x);
       if (seg != c_seg) {
         if (c_seg >= 0) finalize(c_seg);
-        begin_segment(sa + a.q_off);
+        begin_segment(qslots + static_cast<uint32_t>(j) * a.qbuf_bytes);
+        __syncwarp();   // every lane has read the query slot: the producer may refill it
+        if (lane == 0) mbar_arrive(q_empty_bar(bars, W, j));
         c_seg = seg;
       }
       const int tok0 = static_cast<int>(desc.y), len = static_cast<int>(desc.z);
       if (okm != (1u << n) - 1 && lane == 0) flag(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
+      int nv[kChunk];
 #pragma unroll
       for (int i = 0; i < kChunk; ++i)
-        if (i < n) tile(sa + i * a.tile_bytes, ((okm >> i) & 1u) ? min(kTileTokens, len - tok0 - 16 * i) : 0);
+        nv[i] = (i < n && ((okm >> i) & 1u)) ? min(kTileTokens, len - tok0 - 16 * i) : 0;
+      chunk(sa, nv);
     }
     __syncwarp();   // every lane has read the stage: the producer may refill it
     if (lane == 0) mbar_arrive(fb + 8);
@@ -806,23 +901,33 @@ split_kernel(const DecodeArgs a) {
   const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(s_dyn));
   const uint32_t end = base + static_cast<uint32_t>(a.dyn_bytes);
   constexpr uint32_t kLut = lut_bytes<KMODE>();
-  const uint32_t lut = kLut ? lut_at(base, kLut) : end;
+  const uint32_t head = kBarHead + static_cast<uint32_t>(W) * a.qbuf_bytes;
+  const uint32_t lut = kLut ? lut_at(base, kLut, head) : end;
   const uint32_t bars = base;
-  const uint32_t first = base + kBarBytes;
+  const uint32_t qslots = base + kBarHead;
+  const uint32_t first = base + head;
   const bool fits = W >= 1 && W <= kMaxConsumers && (!kLut || lut + kLut <= end) &&
                     stage_at(first, lut, kLut, a.stage_bytes, W * kStages - 1) + a.stage_bytes <= end;
   if (!__syncthreads_and(fits)) {   // launch misconfigured: flag and leave
     if (threadIdx.x == 0) flag(a.status, TQ_DEV_TIMEOUT);
     return;
   }
-  if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent);
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 2 * W * kStages; ++i) mbar_init(bars + 8 * i, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  // The producer starts as soon as the barriers exist; the consumers build the
+  // LUT meanwhile and meet it on named barrier 1 (arrive / sync).
+  if (warp == 0) {
+    const int lane = threadIdx.x & 31;
+    if (lane == 0) {
+      for (int i = 0; i < 2 * W * kStages + W; ++i) mbar_init(bars + 8 * i, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncwarp();
+    asm volatile("bar.arrive 1, %0;\n" ::"r"(blockDim.x) : "memory");
+    producer_warp(a, W, bars, qslots, first, lut, kLut);
+  } else {
+    if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent, threadIdx.x - 32, blockDim.x - 32);
+    asm volatile("bar.sync 1, %0;\n" ::"r"(blockDim.x) : "memory");
+    consumer_warp<KMODE, GBIG, TQ>(a, W, warp - 1, bars, qslots, first, lut, kLut);
   }
-  __syncthreads();   // LUT built, barriers initialised
-  if (warp == 0) producer_warp(a, W, bars, first, lut, kLut);
-  else consumer_warp<KMODE, GBIG, TQ>(a, W, warp - 1, bars, first, lut, kLut);
 }
 
 // ---------------------------------------------------------------- reduce
@@ -968,21 +1073,22 @@ tq_status make_plan(const tq_config* cfg, int batch, int max_seq_len, int bt_str
 struct LaunchShape {
   int consumers;    // consumer warps per CTA (one producer warp besides)
   int stage_bytes;
-  int q_off, desc_off;
+  int desc_off;
   int dyn_bytes;
 };
 
 // Consumer warps whose rings fit around the barrier block and the LUT in a
 // dynamic shared-memory window of `dyn` bytes starting at `start` (the plan
 // the kernel computes); 0 if the LUT itself does not fit.
-int consumers_that_fit(uint32_t start, uint32_t dyn, uint32_t klut, uint32_t sb) {
+int consumers_that_fit(uint32_t start, uint32_t dyn, uint32_t klut, uint32_t sb, uint32_t qbytes) {
   const uint32_t end = start + dyn;
-  const uint32_t lut = klut ? lut_at(start, klut) : end;
-  if (klut && lut + klut > end) return 0;
-  const uint32_t first = start + kBarBytes;
-  int w = kMaxConsumers;
-  while (w > 0 && stage_at(first, lut, klut, sb, w * kStages - 1) + sb > end) --w;
-  return w;
+  for (int w = kMaxConsumers; w > 0; --w) {
+    const uint32_t head = kBarHead + static_cast<uint32_t>(w) * qbytes;
+    const uint32_t lut = klut ? lut_at(start, klut, head) : end;
+    if (klut && lut + klut > end) continue;
+    if (stage_at(start + head, lut, klut, sb, w * kStages - 1) + sb <= end) return w;
+  }
+  return 0;
 }
 
 template <int KMODE>
@@ -990,13 +1096,13 @@ bool launch_shape(int tile_bytes, int group, LaunchShape* s) {
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
-  s->q_off = kChunk * tile_bytes;
-  s->desc_off = s->q_off + group * kD * 2;
+  s->desc_off = kChunk * tile_bytes;
   s->stage_bytes = (s->desc_off + 16 + 127) & ~127;
   const uint32_t klut = lut_bytes<KMODE>();
   // the window may start at 0 or after a small reserved area; take the worse
-  int w = consumers_that_fit(0, optin, klut, s->stage_bytes);
-  const int w2 = consumers_that_fit(1024, optin, klut, s->stage_bytes);
+  const uint32_t qbytes = static_cast<uint32_t>(group) * kD * 2;
+  int w = consumers_that_fit(0, optin, klut, s->stage_bytes, qbytes);
+  const int w2 = consumers_that_fit(1024, optin, klut, s->stage_bytes, qbytes);
   if (w2 < w) w = w2;
   if (w < 1) return false;
   s->consumers = w;
@@ -1009,7 +1115,6 @@ cudaError_t launch_split_typed(DecodeArgs a, cudaStream_t s, int sms) {
   LaunchShape sh;
   if (!launch_shape<KMODE>(a.tile_bytes, a.group, &sh)) return cudaErrorInvalidConfiguration;
   a.stage_bytes = sh.stage_bytes;
-  a.q_off = sh.q_off;
   a.desc_off = sh.desc_off;
   a.dyn_bytes = sh.dyn_bytes;
   a.qbuf_bytes = a.group * kD * 2;
@@ -1086,7 +1191,6 @@ tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* 
   a.cap = P.cap;
   a.tile_bytes = P.L.tile_bytes;
   a.stage_bytes = 0;
-  a.q_off = 0;
   a.desc_off = 0;
   a.k_off = P.L.k_off;
   a.v_off = P.L.v_off;

@@ -1,0 +1,150 @@
+"""Full-size parity in the benchmark's launch configuration, on sampled outputs.
+
+Every workload runs at its full shape with the decode launched exactly as the
+benchmark launches it (whole batch, stream-K split, bf16 output). The oracle
+cannot redo a whole workload, so it checks sampled sequences:
+
+  * store: the GPU-written slots of a sampled sequence against the oracle's
+    quantisation of the same inputs (the store gates of ``parity.py``);
+  * decode: the sampled sequence's blocks are overwritten with the oracle's
+    own bytes, then the GPU decode of the full batch is compared, for a few
+    query heads of that sequence, with the oracle decode of those bytes.
+
+Sampled sequences and the queries come from the CPU generators of
+``workloads`` (the oracle's inputs); the other sequences are generated on the
+device, which only sets the surrounding load.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import codebook as ocb
+from oracle import decode as od
+from oracle import layout as olay
+from oracle import store as ost
+from parity import assert_decode_close, compare_store
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # name: (sampled sequences, sampled query heads)
+    "gqa": ((0, 17, 31), (0, 13, 31)),
+    "k3v4": ((0, 40, 63), (3, 30)),
+    "k8v4": ((5, 127), (0, 21)),
+    "long": ((1,), (0, 37)),
+}
+
+
+@pytest.fixture(scope="module")
+def tq():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need CUDA")
+    from turboquant_paged_kv_gb300 import build
+    build.build()
+    import turboquant_paged_kv_gb300 as tq
+    return tq
+
+
+class _OracleSpec:
+    """Layout, preset and codebook of a workload (what compare_store reads)."""
+
+    def __init__(self, w):
+        self.w = w
+        self.preset = olay.PRESETS[w.preset]
+        self.lay = olay.tile_layout(self.preset, w.d, w.block_size, w.n_kv)
+        if self.preset.key_fp8:
+            self.cent = self.mid = None
+        else:
+            self.cent = ocb.codebook(w.d, self.preset.key_bits)
+            self.mid = ocb.midpoints_fp32(self.cent)
+
+
+def _oracle_sequence_cache(spec, k, v):
+    """Oracle store of one sequence into a compact cache whose block i holds
+    positions [i * bs, (i + 1) * bs)."""
+    length = k.shape[0]
+    nb = (length + spec.lay.block_size - 1) // spec.lay.block_size
+    cache = np.zeros(nb * spec.lay.block_bytes, dtype=np.uint8)
+    for c0 in range(0, length, 16384):
+        c1 = min(length, c0 + 16384)
+        ost.store(k[c0:c1], v[c0:c1], np.arange(c0, c1), cache, spec.lay, spec.preset, spec.cent, spec.mid)
+    return cache
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_fullsize_sampled_parity(tq, name):
+    seqs, heads = CASES[name]
+    w = workloads.get(name)
+    dev = torch.device("cuda", 0)
+    host = workloads.make_inputs(w, "cpu")          # tables, lengths, queries
+    spec = _OracleSpec(w)
+    cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size, partition_tokens=0)
+    bits = {"4bit_nc": 4, "k3v4_nc": 3}.get(w.preset)
+    cb = tq.tq_build_codebook(w.d, bits) if bits else None
+    lay = tq.tq_layout_for(cfg)
+    bb = lay.block_bytes
+    cache = torch.zeros(host.num_blocks * bb, dtype=torch.uint8, device=dev)
+    table = host.block_table.to(dev)
+    lens = host.seq_lens.to(dev)
+    slots = host.fill_slots
+    starts = dict(host.fill_order)
+    sampled_kv = {}
+    for b in range(w.batch):
+        if b in seqs:
+            k, v = host.kv_for_sequence(b, "cpu")
+            sampled_kv[b] = (k, v)
+            k, v = k.to(dev), v.to(dev)
+        else:
+            k, v = host.kv_for_sequence(b, dev)
+        s0 = starts[b]
+        tq.tq_store(cfg, cb, k, v, slots[s0:s0 + k.shape[0]].to(dev), cache)
+    if w.store_tokens:   # the workload's prefill chunk, stored like the benchmark does
+        sk, sv, sslots = host.store_chunk("cpu")
+        tq.tq_store(cfg, cb, sk.to(dev), sv.to(dev), sslots.to(dev), cache)
+    torch.cuda.synchronize()
+
+    blocks = cache.view(host.num_blocks, bb)
+    refs = {}
+    for b in seqs:
+        k, v = (x.double().numpy() for x in sampled_kv[b])
+        length = k.shape[0]
+        ids = host.block_table[b, : (length + w.block_size - 1) // w.block_size].to(torch.int64)
+        # store parity: GPU bytes of this sequence, gathered into compact order
+        gpu_seq = blocks[ids.to(dev)].cpu().numpy().reshape(-1)
+        total = {}
+        for c0 in range(0, length, 16384):   # bounded oracle memory on long sequences
+            c1 = min(length, c0 + 16384)
+            stats = compare_store(gpu_seq, spec, k[c0:c1], v[c0:c1], np.arange(c0, c1))
+            for key, val in stats.items():
+                total[key] = total.get(key, 0) + val
+        print(f"{name} seq {b}: store {total}")
+        # decode input: the oracle's own bytes for this sequence
+        ocache = _oracle_sequence_cache(spec, k, v)
+        blocks[ids.to(dev)] = torch.from_numpy(ocache.reshape(-1, bb)).to(dev)
+        qb = host.q[b:b + 1].double().numpy()
+        refs[b] = od.decode(qb, ocache, spec.lay, spec.preset, spec.cent,
+                            np.arange(len(ids))[None, :], np.array([length]), heads=list(heads))[0]
+    if w.store_tokens:   # prefill chunk: sampled tokens of it, against the oracle
+        sk, sv, sslots = host.store_chunk("cpu")
+        pick = torch.arange(0, sk.shape[0], 97)
+        sblk = (sslots[pick] // w.block_size).to(torch.int64)
+        uniq, inv = torch.unique(sblk, return_inverse=True)
+        gpu_chunk = blocks[uniq.to(dev)].cpu().numpy().reshape(-1)
+        local = inv * w.block_size + sslots[pick] % w.block_size
+        stats = compare_store(gpu_chunk, spec, sk[pick].double().numpy(), sv[pick].double().numpy(), local.numpy())
+        print(f"{name} prefill chunk sample: store {stats}")
+
+    q = host.q.to(dev)
+    out = torch.full((w.batch, w.n_q, w.d), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tq.tq_decode_workspace_size(cfg, w.batch, host.max_seq_len), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    tq.tq_decode(cfg, cb, q, cache, table, lens, host.max_seq_len, out, ws, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    for b in seqs:
+        err = assert_decode_close(got[b, list(heads)], refs[b][list(heads)], torch.bfloat16)
+        print(f"{name} seq {b} heads {heads}: max|gpu - oracle| = {err:.2e}")

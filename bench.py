@@ -125,6 +125,28 @@ def _dist():
     return world, rank, local
 
 
+def rank_workload(rank: int):
+    """Rank ``rank``'s replica of the workload: same shapes, its own seed
+    (weak scaling: every rank decodes a whole batch of its own)."""
+    import workloads
+    return workloads.get(WORKLOAD, seed=rank)
+
+
+def max_over_ranks(values, device, world: int):
+    """Element-wise max of per-rank timings (ms) over all ranks."""
+    import torch
+    vals = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    return vals.tolist()
+
+
+def whole_job_gbs(world: int, bytes_per_rank: int, ms: float) -> float:
+    """Whole-job throughput: bytes all ranks read in one step / the slowest rank's step."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def _oracle_steps(workload: str, steps: int):
     """Time the oracle in a single-threaded child process (spawned, no CUDA):
     one sequence of the workload is oracle-stored once, then each step is the
@@ -201,7 +223,7 @@ def run_tq(args):
     import turboquant_paged_kv_gb300 as tq
     import workloads
 
-    w = workloads.get(WORKLOAD, seed=rank)
+    w = rank_workload(rank)
     inp = workloads.make_inputs(w, device=dev)
     cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size, partition_tokens=args.partition)
     cb = tq.tq_build_codebook(w.d, 4)
@@ -315,15 +337,12 @@ def run_tq(args):
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
     # ---- max over ranks
-    vals = torch.tensor([step_ms, split_ms, store_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
-    step_ms, split_ms, store_ms, e2e_ms = vals.tolist()
+    step_ms, split_ms, store_ms, e2e_ms = max_over_ranks([step_ms, split_ms, store_ms, e2e_ms], dev, world)
     clocks = clk.summary()
 
     if rank == 0:
         peak, peak_src = _peaks()
-        gbs = world * kv_bytes / (step_ms * 1e-3) / 1e9
+        gbs = whole_job_gbs(world, kv_bytes, step_ms)
         split_gbs = kv_bytes / (split_ms * 1e-3) / 1e9
         line = {
             "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -342,7 +361,7 @@ def run_tq(args):
                          "traffic": _profile_traffic("tq_decode.cu", "decode_split_gqa.md"),
                          "peak_source": peak_src, "ms_per_launch": split_ms,
                          "algorithmic_bytes_per_launch": kv_bytes},
-            "e2e": {"value": world * kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "e2e": {"value": whole_job_gbs(world, kv_bytes, e2e_ms), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": 3 * args.steps,
             "clocks": clocks,

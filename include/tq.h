@@ -182,7 +182,11 @@ size_t tq_decode_workspace_size(const tq_config* cfg, int batch, int max_seq_len
  *                16-byte aligned
  *   workspace    device, >= tq_decode_workspace_size bytes, 16-byte aligned;
  *                its contents need no initialisation
- * Launches the split-K kernel then the reduce kernel on `stream`. */
+ * Launches the split-K kernel then the reduce kernel on `stream`.
+ * Like every kernel of this library they are launched with programmatic
+ * dependent launch: each may be scheduled while the previous kernel in the
+ * stream finishes, and waits for it (griddepcontrol.wait) before touching
+ * any global memory, so stream order is kept for all arguments. */
 tq_status tq_decode(const tq_config* cfg, const tq_codebook* cb,
                     const void* q, int q_dtype,
                     const void* cache, long long num_blocks,

@@ -37,7 +37,8 @@ def _sources():
 
 
 def _deps():
-    return _sources() + [os.path.join(CSRC, "tq_internal.h"), os.path.join(INCLUDE, "tq.h"),
+    return _sources() + [os.path.join(CSRC, "tq_internal.h"), os.path.join(CSRC, "tq_launch.cuh"),
+                         os.path.join(INCLUDE, "tq.h"),
                          os.path.abspath(__file__)]
 
 

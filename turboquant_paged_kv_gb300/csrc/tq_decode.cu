@@ -83,6 +83,7 @@
 #include <type_traits>
 
 #include "tq_internal.h"
+#include "tq_launch.cuh"
 
 namespace tq {
 namespace {
@@ -909,11 +910,15 @@ split_kernel(const DecodeArgs a) {
   const bool fits = W >= 1 && W <= kMaxConsumers && (!kLut || lut + kLut <= end) &&
                     stage_at(first, lut, kLut, a.stage_bytes, W * kStages - 1) + a.stage_bytes <= end;
   if (!__syncthreads_and(fits)) {   // launch misconfigured: flag and leave
+    grid_dep_wait();
     if (threadIdx.x == 0) flag(a.status, TQ_DEV_TIMEOUT);
     return;
   }
-  // The producer starts as soon as the barriers exist; the consumers build the
-  // LUT meanwhile and meet it on named barrier 1 (arrive / sync).
+  // Barrier init and the LUT (from kernel parameters) touch no global memory,
+  // so they overlap the end of the previous kernel; everything after
+  // grid_dep_wait() may read what that kernel wrote. The producer starts as
+  // soon as the barriers exist; the consumers build the LUT meanwhile and meet
+  // it on named barrier 1 (arrive / sync).
   if (warp == 0) {
     const int lane = threadIdx.x & 31;
     if (lane == 0) {
@@ -921,11 +926,15 @@ split_kernel(const DecodeArgs a) {
       asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     __syncwarp();
+    grid_dep_wait();
+    grid_dep_launch();
     asm volatile("bar.arrive 1, %0;\n" ::"r"(blockDim.x) : "memory");
     producer_warp(a, W, bars, qslots, first, lut, kLut);
   } else {
     if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent, threadIdx.x - 32, blockDim.x - 32);
     asm volatile("bar.sync 1, %0;\n" ::"r"(blockDim.x) : "memory");
+    grid_dep_wait();   // already resolved: the producer passed it before arriving
+    grid_dep_launch();
     consumer_warp<KMODE, GBIG, TQ>(a, W, warp - 1, bars, qslots, first, lut, kLut);
   }
 }
@@ -958,6 +967,8 @@ __global__ void __launch_bounds__(kD) reduce_kernel(const ReduceArgs a) {
   const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31;
   const int G = a.group;
   const int h = hq / G, gg = hq - h * G;
+  grid_dep_wait();   // records (and everything else) come from earlier kernels
+  grid_dep_launch();
   if (d < 32) {   // tiles before sequence b, and in total; the length of b
     long long before = 0, total = 0;
     for (int b0 = 0; b0 < a.batch; b0 += 32) {
@@ -1121,8 +1132,8 @@ cudaError_t launch_split_typed(DecodeArgs a, cudaStream_t s, int sms) {
   auto k = split_kernel<KMODE, GBIG, TQ>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, a.dyn_bytes);
   if (err != cudaSuccess) return err;
-  k<<<static_cast<unsigned>(sms), (sh.consumers + 1) * 32, static_cast<size_t>(a.dyn_bytes), s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(static_cast<unsigned>(sms)), dim3((sh.consumers + 1) * 32),
+                    static_cast<size_t>(a.dyn_bytes), s, a);
 }
 
 template <int KMODE>
@@ -1242,10 +1253,11 @@ tq_status run_reduce(const tq_config* cfg, const int* seq_lens, int batch, int m
   r.cap = P.cap;
   r.num_warps = P.sms * warps;
   const dim3 grid(static_cast<unsigned>(cfg->num_q_heads), static_cast<unsigned>(batch));
-  if (out_dtype == TQ_DTYPE_F32) reduce_kernel<float><<<grid, kD, 0, stream>>>(r);
-  else if (out_dtype == TQ_DTYPE_F16) reduce_kernel<__half><<<grid, kD, 0, stream>>>(r);
-  else reduce_kernel<__nv_bfloat16><<<grid, kD, 0, stream>>>(r);
-  return cudaGetLastError() == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
+  cudaError_t err;
+  if (out_dtype == TQ_DTYPE_F32) err = launch_pdl(reduce_kernel<float>, grid, dim3(kD), 0, stream, r);
+  else if (out_dtype == TQ_DTYPE_F16) err = launch_pdl(reduce_kernel<__half>, grid, dim3(kD), 0, stream, r);
+  else err = launch_pdl(reduce_kernel<__nv_bfloat16>, grid, dim3(kD), 0, stream, r);
+  return err == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
 }  // namespace

@@ -28,6 +28,7 @@
 #include <type_traits>
 
 #include "tq_internal.h"
+#include "tq_launch.cuh"
 
 namespace tq {
 namespace {
@@ -111,6 +112,8 @@ __device__ __forceinline__ void flag(unsigned int* status, unsigned int bit) {
 template <int KMODE, typename T>
 __global__ void __launch_bounds__(kStoreWarps * 32)
 store_kernel(const StoreArgs a) {
+  grid_dep_wait();   // inputs and cache may come from the previous kernel
+  grid_dep_launch();
   __shared__ float s_cent[16];
   if (threadIdx.x < 16) s_cent[threadIdx.x] = a.cent[threadIdx.x];
   __syncthreads();
@@ -211,11 +214,14 @@ store_kernel(const StoreArgs a) {
 template <int KMODE>
 cudaError_t launch_store(const StoreArgs& a, int in_dtype, cudaStream_t stream) {
   const long long blocks = (a.num_vectors + kStoreWarps - 1) / kStoreWarps;
+  cudaError_t err;
   if (in_dtype == TQ_DTYPE_BF16)
-    store_kernel<KMODE, __nv_bfloat16><<<static_cast<unsigned>(blocks), kStoreWarps * 32, 0, stream>>>(a);
+    err = launch_pdl(store_kernel<KMODE, __nv_bfloat16>, dim3(static_cast<unsigned>(blocks)), dim3(kStoreWarps * 32), 0,
+                     stream, a);
   else
-    store_kernel<KMODE, __half><<<static_cast<unsigned>(blocks), kStoreWarps * 32, 0, stream>>>(a);
-  return cudaGetLastError();
+    err = launch_pdl(store_kernel<KMODE, __half>, dim3(static_cast<unsigned>(blocks)), dim3(kStoreWarps * 32), 0,
+                     stream, a);
+  return err;
 }
 
 }  // namespace

@@ -652,39 +652,59 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
     }
   };
 
-  // query rows of a new segment: rotate, scale, split hi/lo, scatter into B operands
+  // query rows of a new segment: rotate, scale, split hi/lo, and place into the
+  // B operands through the query slot itself. Each lane overwrites its own 8
+  // bytes of every raw row with the hi parts (row = head, fp16), keeping the lo
+  // parts in registers; each lane then loads its operand column (column g,
+  // coordinates 32c .. 32c + 31: one 64-byte run); then the same for the lo
+  // parts.
   auto begin_segment = [&](uint32_t qrows) {
-#pragma unroll
-    for (int i = 0; i < (GBIG ? 32 : 16); ++i) qb[i] = 0u;
+    uint32_t lo[8][2];   // per head: lo01, lo23 of coordinates 4 lane .. +3
 #pragma unroll
     for (int gg = 0; gg < 8; ++gg) {
       if (gg < G) {
+        const uint32_t at = qrows + gg * kD * 2 + 8 * lane;
         float x[4];
-        u2_to_f4<TQ>(lds64(qrows + gg * kD * 2 + 8 * lane), x);
+        u2_to_f4<TQ>(lds64(at), x);
         float sc = a.qscale;
         if constexpr (KMODE != kFp8) {
           fwht128(x, lane);
           sc *= 0.088388347648318440f;   // 1 / sqrt(128)
         }
-        uint32_t hp[4];   // hi01, lo01, hi23, lo23 of coordinates 4 lane .. +3
-        split_half2(x[0] * sc, x[1] * sc, hp[0], hp[1]);
-        split_half2(x[2] * sc, x[3] * sc, hp[2], hp[3]);
-        // B column g takes head gg's hi part (g == gg) or lo part (g == gg + 4)
-        const bool take_hi = g == gg, take_lo = GBIG ? (g == gg) : (g == gg + 4);
+        uint32_t h01, h23;
+        split_half2(x[0] * sc, x[1] * sc, h01, lo[gg][0]);
+        split_half2(x[2] * sc, x[3] * sc, h23, lo[gg][1]);
+        sts64(at, make_uint2(h01, h23));
+      }
+    }
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {   // coordinates 32c + 4s .. +3 live in lane 8c + s
-          const uint32_t h01 = __shfl_sync(0xffffffffu, hp[0], 8 * c + s);
-          const uint32_t l01 = __shfl_sync(0xffffffffu, hp[1], 8 * c + s);
-          const uint32_t h23 = __shfl_sync(0xffffffffu, hp[2], 8 * c + s);
-          const uint32_t l23 = __shfl_sync(0xffffffffu, hp[3], 8 * c + s);
-          if (GBIG) {
-            if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; qb[16 + 2 * s] = l01; qb[16 + 2 * s + 1] = l23; }
-          } else {
-            if (take_hi) { qb[2 * s] = h01; qb[2 * s + 1] = h23; }
-            if (take_lo) { qb[2 * s] = l01; qb[2 * s + 1] = l23; }
-          }
+    for (int part = 0; part < 2; ++part) {   // 0: hi parts, 1: lo parts
+      if (part == 1) {
+#pragma unroll
+        for (int gg = 0; gg < 8; ++gg)
+          if (gg < G) sts64(qrows + gg * kD * 2 + 8 * lane, make_uint2(lo[gg][0], lo[gg][1]));
+      }
+      __syncwarp();
+      // column g of the B operand: G <= 4: hi of head g (g < 4), lo of head
+      // g - 4 (g >= 4); G > 4: head g, hi then lo in the second register half
+      const int row = GBIG ? g : (part == 0 ? g : g - 4);
+      const bool mine = GBIG ? (g < G) : (part == 0 ? g < G : (g >= 4 && g - 4 < G));
+      uint4 r[4] = {};
+      if (mine) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) r[k] = lds128(qrows + row * kD * 2 + 64 * c + 16 * k);
+      }
+      const int base = GBIG ? 16 * part : 0;
+      if (GBIG || mine || part == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          qb[base + 4 * k] = r[k].x;
+          qb[base + 4 * k + 1] = r[k].y;
+          qb[base + 4 * k + 2] = r[k].z;
+          qb[base + 4 * k + 3] = r[k].w;
         }
       }
+      __syncwarp();   // every lane has read this part before the next overwrites it
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;

@@ -972,24 +972,33 @@ __device__ __forceinline__ int reduce_len(const ReduceArgs& a, int b) {
   return min(max(__ldg(a.seq_lens + b), 0), min(a.max_seq_len, a.cap));
 }
 
-// One CTA per (query head, sequence), thread d = coordinate. The records of a
-// segment are those of the consumer warps whose ranges overlap it, a
-// contiguous warp range; every thread walks that range 16 warps at a time,
-// loads the LSEs and its partial coordinates of all of them at once (record 0
-// stands in for a warp whose range is empty, and a select, not a multiply,
-// drops it: the workspace may hold any bits), and merges them online.
-constexpr int kReduceChunk = 16;
-
+// One CTA per (sequence, KV head); thread (gg, d) = query head gg of the
+// group, coordinate d. The records of a segment are those of the consumer
+// warps whose ranges overlap it, a contiguous warp range. Warp 0 computes
+// that range (the only divisions), then walks it 32 warps at a time, one
+// candidate per lane: whether the warp owns a tile at all, its record, and
+// the record's LSE for every head; it publishes merge weights per (candidate,
+// head). Every thread then adds its coordinate of the weighted partials
+// (record 0 stands in for a warp whose range is empty, and a select, not a
+// multiply, drops it: the workspace may hold any bits). Chunks of candidates
+// and partitions are merged online.
 template <typename TO>
-__global__ void __launch_bounds__(kD) reduce_kernel(const ReduceArgs a) {
+__global__ void __launch_bounds__(8 * kD) reduce_kernel(const ReduceArgs a) {
   __shared__ long long s_pre[2];
+  __shared__ long long s_wf[32], s_wl[32], s_q[32], s_r[32];
   __shared__ int s_len;
-  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x, lane = d & 31;
+  __shared__ int s_rec[32];
+  __shared__ float s_w[32][8];
+  __shared__ float s_alpha[8];
+  __shared__ int s_cnt;
+  const int h = blockIdx.x, b = blockIdx.y;
   const int G = a.group;
-  const int h = hq / G, gg = hq - h * G;
+  const int gg = threadIdx.x / kD, d = threadIdx.x - gg * kD;
+  const int lane = threadIdx.x & 31;
+  const bool w0 = threadIdx.x < 32;
   grid_dep_wait();   // records (and everything else) come from earlier kernels
   grid_dep_launch();
-  if (d < 32) {   // tiles before sequence b, and in total; the length of b
+  if (w0) {   // tiles before sequence b, and in total; the length of b
     long long before = 0, total = 0;
     for (int b0 = 0; b0 < a.batch; b0 += 32) {
       const int j = b0 + lane;
@@ -1004,57 +1013,87 @@ __global__ void __launch_bounds__(kD) reduce_kernel(const ReduceArgs a) {
       total += nt;
       before += nb;
     }
-    if (d == 0) { s_pre[0] = before * a.n_kv; s_pre[1] = total * a.n_kv; }
+    if (lane == 0) { s_pre[0] = before * a.n_kv; s_pre[1] = total * a.n_kv; }
   }
   __syncthreads();
-  const long long orow = static_cast<long long>(b) * a.n_q + hq;
+  const long long orow = static_cast<long long>(b) * a.n_q + static_cast<long long>(h) * G + gg;
   const int len = s_len;
   if (len <= 0) { store_out<TO>(a.out, orow * kD + d, 0.f); return; }
   const int nt = (len + kTileTokens - 1) / kTileTokens;
   const long long T = s_pre[1], nw = a.num_warps;
-  const long long Tq = T / nw, Tr = T - Tq * nw;   // warp w owns tiles [T w / nw, T (w + 1) / nw)
   const long long seq0 = s_pre[0] + static_cast<long long>(h) * nt;   // first tile of (b, h)
   const int ppt = a.part_tiles > 0 ? a.part_tiles : nt;
   const int parts = (nt + ppt - 1) / ppt;
-  float acc = 0.f, den = 0.f, mx = -INFINITY;
-  for (int p = 0; p < parts; ++p) {
-    const long long t0 = seq0 + static_cast<long long>(p) * ppt;
-    const long long t1 = seq0 + min(static_cast<long long>(p + 1) * ppt, static_cast<long long>(nt));
-    const long long seg = (static_cast<long long>(b) * a.n_kv + h) * a.num_parts + p;
-    const long long wf = ((t0 + 1) * nw - 1) / T, wl = (t1 * nw - 1) / T;
-    for (long long wb = wf; wb <= wl; wb += kReduceChunk) {
-      const int cnt = static_cast<int>(min(static_cast<long long>(kReduceChunk), wl - wb + 1));
-      long long q = T * wb / nw, r = T * wb - q * nw;   // first tile of warp wb, and remainder
-      float lse[kReduceChunk], x[kReduceChunk];
+  long long Tq = 0, Tr = 0;   // warp w owns tiles [T w / nw, T (w + 1) / nw); T = Tq nw + Tr
+  if (w0) {
+    Tq = T / nw;
+    Tr = T - Tq * nw;
+  }
+  float acc = 0.f, den = 0.f;
+  float mxh[8];   // warp 0: running LSE max per head
 #pragma unroll
-      for (int i = 0; i < kReduceChunk; ++i) {
-        lse[i] = -INFINITY;
-        x[i] = 0.f;
-        if (i < cnt) {
-          long long nq = q + Tq, nr = r + Tr;
-          if (nr >= nw) { nr -= nw; ++nq; }
-          const bool ok = nq != q;   // warp wb + i owns at least one tile
-          q = nq;
-          r = nr;
-          const long long rec = ok ? seg + wb + i : 0;
-          if (ok) lse[i] = a.rec_lse[rec * G + gg];
-          x[i] = a.rec_o[(rec * G + gg) * kD + d];
-        }
-      }
-      float nm = mx;
-#pragma unroll
-      for (int i = 0; i < kReduceChunk; ++i) nm = fmaxf(nm, lse[i]);
-      const float al = mx == -INFINITY ? 0.f : exp2f(mx - nm);
-      acc *= al;
-      den *= al;
-#pragma unroll
-      for (int i = 0; i < kReduceChunk; ++i) {
-        const float w = lse[i] == -INFINITY ? 0.f : exp2f(lse[i] - nm);
-        den += w;
-        acc = w != 0.f ? fmaf(w, x[i], acc) : acc;
-      }
-      mx = nm;
+  for (int k = 0; k < 8; ++k) mxh[k] = -INFINITY;
+  for (int p0 = 0; p0 < parts; p0 += 32) {
+    if (w0 && p0 + lane < parts) {   // contributing warps of partition p0 + lane
+      const int p = p0 + lane;
+      const long long t0 = seq0 + static_cast<long long>(p) * ppt;
+      const long long t1 = seq0 + min(static_cast<long long>(p + 1) * ppt, static_cast<long long>(nt));
+      const long long wf = ((t0 + 1) * nw - 1) / T, wl = (t1 * nw - 1) / T;
+      const long long q = T * wf / nw;
+      s_wf[lane] = wf;
+      s_wl[lane] = wl;
+      s_q[lane] = q;
+      s_r[lane] = T * wf - q * nw;
     }
+    __syncthreads();
+    const int pend = min(parts - p0, 32);
+    for (int pi = 0; pi < pend; ++pi) {
+      const long long seg = (static_cast<long long>(b) * a.n_kv + h) * a.num_parts + p0 + pi;
+      const long long wf = s_wf[pi], wl = s_wl[pi];
+      long long q0 = s_q[pi], r0 = s_r[pi];   // first tile of warp wb, and remainder
+      for (long long wb = wf; wb <= wl; wb += 32) {
+        if (w0) {
+          // candidate wb + lane starts at tile q0 + lane Tq + floor((r0 + lane Tr) / nw)
+          const long long i = lane;
+          const long long rr = r0 + i * Tr, rn = rr + Tr;
+          const long long qi = q0 + i * Tq + rr / nw;
+          const long long qn = q0 + (i + 1) * Tq + rn / nw;
+          const bool ok = wb + i <= wl && qn != qi;   // warp wb + i owns at least one tile
+          const long long rec = seg + wb + i;
+          s_rec[lane] = ok ? static_cast<int>(rec) : 0;
+          if (lane == 0) s_cnt = static_cast<int>(min(32ll, wl - wb + 1));
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (k < G) {
+              const float lse = ok ? a.rec_lse[rec * G + k] : -INFINITY;
+              float cm = lse;
+              for (int o = 1; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+              const float nm = fmaxf(mxh[k], cm);
+              s_w[lane][k] = lse == -INFINITY ? 0.f : exp2f(lse - nm);
+              if (lane == 0) s_alpha[k] = mxh[k] == -INFINITY ? 0.f : exp2f(mxh[k] - nm);
+              mxh[k] = nm;
+            }
+          }
+          const long long r32 = r0 + 32 * Tr;   // the next 32 candidates
+          q0 += 32 * Tq + r32 / nw;
+          r0 = r32 % nw;
+        }
+        __syncthreads();
+        const int cnt = s_cnt;
+        const float al = s_alpha[gg];
+        acc *= al;
+        den *= al;
+#pragma unroll 4
+        for (int i = 0; i < cnt; ++i) {
+          const float wgt = s_w[i][gg];
+          const float x = a.rec_o[(static_cast<long long>(s_rec[i]) * G + gg) * kD + d];
+          den += wgt;
+          acc = wgt != 0.f ? fmaf(wgt, x, acc) : acc;
+        }
+        __syncthreads();   // weights used before warp 0 writes the next chunk's
+      }
+    }
+    __syncthreads();   // this group's ranges are used before warp 0 writes the next
   }
   store_out<TO>(a.out, orow * kD + d, den > 0.f ? acc / den : 0.f);
 }
@@ -1272,11 +1311,12 @@ tq_status run_reduce(const tq_config* cfg, const int* seq_lens, int batch, int m
   r.max_seq_len = max_seq_len;
   r.cap = P.cap;
   r.num_warps = P.sms * warps;
-  const dim3 grid(static_cast<unsigned>(cfg->num_q_heads), static_cast<unsigned>(batch));
+  const dim3 grid(static_cast<unsigned>(cfg->num_kv_heads), static_cast<unsigned>(batch));
   cudaError_t err;
-  if (out_dtype == TQ_DTYPE_F32) err = launch_pdl(reduce_kernel<float>, grid, dim3(kD), 0, stream, r);
-  else if (out_dtype == TQ_DTYPE_F16) err = launch_pdl(reduce_kernel<__half>, grid, dim3(kD), 0, stream, r);
-  else err = launch_pdl(reduce_kernel<__nv_bfloat16>, grid, dim3(kD), 0, stream, r);
+  const dim3 block(static_cast<unsigned>(G * kD));
+  if (out_dtype == TQ_DTYPE_F32) err = launch_pdl(reduce_kernel<float>, grid, block, 0, stream, r);
+  else if (out_dtype == TQ_DTYPE_F16) err = launch_pdl(reduce_kernel<__half>, grid, block, 0, stream, r);
+  else err = launch_pdl(reduce_kernel<__nv_bfloat16>, grid, block, 0, stream, r);
   return err == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

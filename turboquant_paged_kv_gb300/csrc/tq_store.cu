@@ -46,6 +46,7 @@ struct StoreArgs {
   long long num_blocks;
   int n_kv;
   int block_size;
+  int log2_bs;               // block_size is a power of two
   int tiles_per_block;
   int tile_bytes;
   int k_off, k_row;
@@ -78,16 +79,6 @@ __device__ __forceinline__ float warp_sum(float x) {
   for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
   return x;
 }
-__device__ __forceinline__ float warp_min(float x) {
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, m));
-  return x;
-}
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, m));
-  return x;
-}
 
 // Sylvester-order Walsh-Hadamard transform of the 128 coordinates held as
 // 4 consecutive values per lane (coordinate 4*lane + j).
@@ -114,19 +105,25 @@ __global__ void __launch_bounds__(kStoreWarps * 32)
 store_kernel(const StoreArgs a) {
   grid_dep_wait();   // inputs and cache may come from the previous kernel
   grid_dep_launch();
-  __shared__ float s_cent[16];
-  if (threadIdx.x < 16) s_cent[threadIdx.x] = a.cent[threadIdx.x];
+  __shared__ float s_cent[16], s_mid[16];
+  if (threadIdx.x < 16) {
+    s_cent[threadIdx.x] = a.cent[threadIdx.x];
+    s_mid[threadIdx.x] = threadIdx.x < 15 ? a.mid[threadIdx.x] : 0.f;
+  }
   __syncthreads();
 
   const int lane = threadIdx.x & 31;
   const long long vec = static_cast<long long>(blockIdx.x) * kStoreWarps + (threadIdx.x >> 5);
   if (vec >= a.num_vectors) return;
-  const long long tok = vec / a.n_kv;
+  // vec / n_kv in 32 bits whenever the vector count allows
+  const long long tok = a.num_vectors < (1ll << 32)
+                            ? static_cast<long long>(static_cast<unsigned>(vec) / static_cast<unsigned>(a.n_kv))
+                            : vec / a.n_kv;
   const int head = static_cast<int>(vec - tok * a.n_kv);
   const long long slot = a.slots[tok];
   if (slot < 0) return;
-  const long long blk = slot / a.block_size;
-  const int off = static_cast<int>(slot - blk * a.block_size);
+  const long long blk = slot >> a.log2_bs;
+  const int off = static_cast<int>(slot & (a.block_size - 1));
   if (blk >= a.num_blocks) {
     if (lane == 0) flag(a.status, TQ_DEV_SLOT_OUT_OF_RANGE);
     return;
@@ -158,9 +155,10 @@ store_kernel(const StoreArgs a) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float y = k[j] * sc;
+      // #{m : y >= mid_m} over the ascending midpoints, by binary search
       int c = 0;
 #pragma unroll
-      for (int m = 0; m < (1 << KMODE) - 1; ++m) c += (y >= a.mid[m]) ? 1 : 0;
+      for (int step = 1 << (KMODE - 1); step >= 1; step >>= 1) c += (y >= s_mid[c + step - 1]) ? step : 0;
       idx[j] = c;
       const float cv = s_cent[c];
       cs = fmaf(cv, cv, cs);
@@ -188,8 +186,8 @@ store_kernel(const StoreArgs a) {
   // ---------------- values (4-bit) ----------------
   float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
   float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-  mn = warp_min(mn);
-  mx = warp_max(mx);
+  asm("redux.sync.min.f32 %0, %0, 0xffffffff;" : "+f"(mn));
+  asm("redux.sync.max.f32 %0, %0, 0xffffffff;" : "+f"(mx));
   float s = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
   s = (s > 1e-8f) ? s : 1e-8f;
   uint32_t w = 0;
@@ -260,6 +258,7 @@ extern "C" tq_status tq_store(const tq_config* cfg, const tq_codebook* cb,
   a.num_blocks = num_blocks;
   a.n_kv = cfg->num_kv_heads;
   a.block_size = cfg->block_size;
+  a.log2_bs = __builtin_ctz(static_cast<unsigned>(cfg->block_size));
   a.tiles_per_block = cfg->block_size / kTileTokens;
   a.tile_bytes = L.tile_bytes;
   a.k_off = L.k_off;

@@ -190,10 +190,18 @@ store_kernel(const StoreArgs a) {
   asm("redux.sync.max.f32 %0, %0, 0xffffffff;" : "+f"(mx));
   float s = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
   s = (s > 1e-8f) ? s : 1e-8f;
+  // code = trunc(fp32((v - min) / s) + 1/2) with IEEE division, as specified.
+  // The product with the correctly rounded reciprocal is within 4e-6 of it
+  // (t <= 15), so away from a rounding boundary it gives the same code; within
+  // 1e-5 of one the exact quotient is taken.
+  const float rs = __frcp_rn(s);
   uint32_t w = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    int q = __float2int_rz(__fadd_rn(__fdiv_rn(__fsub_rn(v[j], mn), s), 0.5f));
+    const float dv = __fsub_rn(v[j], mn);
+    const float u = __fadd_rn(__fmul_rn(dv, rs), 0.5f);
+    const float fr = u - floorf(u);
+    int q = (fr < 1e-5f || fr > 1.f - 1e-5f) ? __float2int_rz(__fadd_rn(__fdiv_rn(dv, s), 0.5f)) : __float2int_rz(u);
     q = min(max(q, 0), 15);
     w |= static_cast<uint32_t>(q) << (4 * j);
   }

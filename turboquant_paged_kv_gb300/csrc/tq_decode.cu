@@ -941,10 +941,8 @@ split_kernel(const DecodeArgs a) {
   // it on named barrier 1 (arrive / sync).
   if (warp == 0) {
     const int lane = threadIdx.x & 31;
-    if (lane == 0) {
-      for (int i = 0; i < 2 * W * kStages + W; ++i) mbar_init(bars + 8 * i, 1);
-      asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
+    for (int i = lane; i < 2 * W * kStages + W; i += 32) mbar_init(bars + 8 * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     __syncwarp();
     grid_dep_wait();
     grid_dep_launch();

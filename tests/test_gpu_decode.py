@@ -55,10 +55,13 @@ def gpu_decode(tq, w, inp, cache_np, out_dtype=torch.float32, partition_tokens=N
     return out.float().cpu().numpy()
 
 
+# partition_tokens None: the workload's own (fixed partitions, split + reduce
+# kernels); 0: stream-K, where tq_decode merges in the split kernel itself
+@pytest.mark.parametrize("pt", [None, 0])
 @pytest.mark.parametrize("name", ["tiny", "gqa_small", "k3v4_small", "k8v4_small", "long_small"])
-def test_decode_matches_oracle_f32(tq, name):
+def test_decode_matches_oracle_f32(tq, name, pt):
     w, inp, oc, q, ref = oracle_case(name)
-    got = gpu_decode(tq, w, inp, oc.cache)
+    got = gpu_decode(tq, w, inp, oc.cache, partition_tokens=pt)
     err = assert_decode_close(got, ref, torch.float32)
     assert err < 1e-3
     # reported, not gated: agreement with unquantised attention
@@ -66,11 +69,12 @@ def test_decode_matches_oracle_f32(tq, name):
     print(f"{name}: max|gpu-oracle| = {err:.2e}, cos(oracle, unquantised) = {cos:.5f}")
 
 
+@pytest.mark.parametrize("pt", [None, 0])
 @pytest.mark.parametrize("name", ["tiny", "gqa_small", "long_small"])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
-def test_decode_matches_oracle_16bit_out(tq, name, dtype):
+def test_decode_matches_oracle_16bit_out(tq, name, dtype, pt):
     w, inp, oc, q, ref = oracle_case(name)
-    got = gpu_decode(tq, w, inp, oc.cache, out_dtype=dtype)
+    got = gpu_decode(tq, w, inp, oc.cache, out_dtype=dtype, partition_tokens=pt)
     assert_decode_close(got, ref, dtype)
 
 
@@ -96,13 +100,14 @@ def test_decode_block_sizes(tq, bs):
     assert_decode_close(got, ref, torch.float32)
 
 
-def test_decode_empty_and_single_token_sequences(tq):
+@pytest.mark.parametrize("pt", [None, 0])
+def test_decode_empty_and_single_token_sequences(tq, pt):
     w, inp, oc, q, _ = oracle_case("gqa_small")
     lens = inp.seq_lens.clone()
     lens[0] = 0
     lens[2] = 1
     ref = oc.decode(q, seq_lens=lens.numpy())
-    got = gpu_decode(tq, w, inp, oc.cache, seq_lens=lens, max_seq_len=int(inp.seq_lens.max()))
+    got = gpu_decode(tq, w, inp, oc.cache, seq_lens=lens, max_seq_len=int(inp.seq_lens.max()), partition_tokens=pt)
     assert np.all(got[0] == 0.0)
     assert_decode_close(got, ref, torch.float32)
 
@@ -160,3 +165,11 @@ def test_gpu_store_then_decode_end_to_end(tq):
     tq.tq_store(cfg, cb, k, v, inp.fill_slots.cuda(), cache)
     got = gpu_decode(tq, w, inp, cache.cpu().numpy())
     assert_decode_close(got, ref, torch.float32)
+
+
+@pytest.mark.parametrize("pt", [None, 0])
+def test_decode_all_sequences_empty(tq, pt):
+    w, inp, oc, q, _ = oracle_case("gqa_small")
+    lens = torch.zeros_like(inp.seq_lens)
+    got = gpu_decode(tq, w, inp, oc.cache, seq_lens=lens, max_seq_len=16, partition_tokens=pt)
+    assert np.all(got == 0.0)

@@ -416,6 +416,16 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
   const long long nw = static_cast<long long>(gridDim.x) * W;
   const long long wid = static_cast<long long>(blockIdx.x) * W + lane;
 
+  // the block table is read block id by block id below: start it towards L2
+  // now, spread over the grid (at most 16 MB of table)
+  {
+    const long long bt_bytes = min(static_cast<long long>(a.batch) * a.bt_stride * 4, 16ll << 20);
+    const char* bt = reinterpret_cast<const char*>(a.block_table);
+    for (long long off = (static_cast<long long>(blockIdx.x) * 32 + lane) * 128; off < bt_bytes;
+         off += static_cast<long long>(gridDim.x) * 32 * 128)
+      asm volatile("prefetch.global.L2 [%0];\n" ::"l"(bt + off));
+  }
+
   // tiles of the whole line: n_kv * sum_b ceil(len_b / 16)
   long long total = 0;
   bool too_long = false;
@@ -435,8 +445,15 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
   }
   if (blockIdx.x == 0 && __any_sync(0xffffffffu, too_long) && lane == 0) flag(a.status, TQ_DEV_SEQ_TOO_LONG);
   total *= a.n_kv;
-  const long long r0 = mine ? total * wid / nw : 0;
-  long long rem = mine ? total * (wid + 1) / nw - r0 : 0;   // tiles left to plan
+  // range [total * wid / nw, total * (wid + 1) / nw), 32-bit division when it fits
+  const bool narrow = total * nw < (1ll << 32);
+  const long long r0 = !mine ? 0 : narrow ? static_cast<long long>(static_cast<unsigned>(total * wid) /
+                                                                   static_cast<unsigned>(nw))
+                                          : total * wid / nw;
+  const long long r1 = !mine ? 0 : narrow ? static_cast<long long>(static_cast<unsigned>(total * (wid + 1)) /
+                                                                   static_cast<unsigned>(nw))
+                                          : total * (wid + 1) / nw;
+  long long rem = r1 - r0;   // tiles left to plan
 
   // locate r0: per group of 32 sequences an inclusive scan of their tile
   // counts, then a per-lane binary search over it

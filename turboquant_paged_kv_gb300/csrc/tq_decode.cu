@@ -43,19 +43,18 @@
 //  Math. Both contractions run on tensor cores with mma.sync.m16n8k16 (f16 in,
 //  f32 accumulate; one such mma occupies a sub-partition's tensor pipe for
 //  about 8 cycles on GB300, so the layout wastes as few rows as possible):
-//    S[8 tok x 2 parts, 8] = K . Q^T. Rows g and 8 + g hold token g with the
-//      centroid hi and lo parts (c = c_hi + c_lo in fp16); one 8-byte LUT entry
-//      per key byte (16 copies, one per lane of a half warp, so lookups never
-//      conflict; the table is aligned so one PRMT forms the address) is exactly
-//      the (row g,
-//      row 8 + g) operand pair, and the two rows are summed in the same lane.
-//      The 2 tiles of a chunk run in lock step, so 4 accumulation chains
-//      interleave.
+//    S[16 tok, 8] = K . Q^T. Rows are the tile's 16 tokens. The centroids are
+//      held as c' = fp16(gamma c), gamma a per-codebook scale in [1, 2) chosen
+//      on the host so that no centroid rounds by more than ~1e-4 relative
+//      (the query is divided by gamma). One 4-byte LUT entry per key byte
+//      gives a half2 of its two centroids (32 copies, one per lane, so
+//      lookups never conflict; the table is aligned so one PRMT forms the
+//      address). The 2 tiles of a chunk run in lock step with two
+//      accumulators each, so 4 accumulation chains interleave.
 //      Columns 0..3 hold q_hi of the G <= 4 query heads and columns 4..7 q_lo of
 //      the same heads (q = q_hi + q_lo), so one mma per 16 coordinates covers
-//      all products to ~2^-22 relative (fp16 operands alone miss the 2e-3
-//      output gate), and lanes c, c ^ 2 of a quad hold the hi and lo parts of
-//      the same heads: one exchange completes the score. For G > 4 the q_lo
+//      the query to ~2^-22 relative, and lanes c, c ^ 2 of a quad hold the hi
+//      and lo parts of the same heads: one exchange completes the score. For G > 4 the q_lo
 //      columns take a second mma.
 //    P^T reaches the B-operand layout through movmatrix.trans (the S layout has
 //      tokens in rows), one instruction per 8x8 block of fp16 hi or lo parts.
@@ -80,6 +79,8 @@
 #include <stdint.h>
 
 #include <climits>
+#include <cmath>
+#include <mutex>
 #include <type_traits>
 
 #include "tq_internal.h"
@@ -185,6 +186,9 @@ __device__ __forceinline__ float lds_h2f(uint32_t a) {   // one fp16 -> float
   unsigned short v;
   asm volatile("ld.shared.u16 %0, [%1];\n" : "=h"(v) : "r"(a));
   return __half2float(__ushort_as_half(v));
+}
+__device__ __forceinline__ void sts32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(a), "r"(v));
 }
 __device__ __forceinline__ void sts64(uint32_t a, uint2 v) {
   asm volatile("st.shared.v2.u32 [%0], {%1,%2};\n" ::"r"(a), "r"(v.x), "r"(v.y));
@@ -295,13 +299,13 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 
 // ---------------------------------------------------------------- LUT
 
-// Entry e (a key byte, or a 6-bit pair of 3-bit indices) holds 16 copies of
-// uint2 {half2(c_hi[lo idx], c_hi[hi idx]), half2(c_lo[..], c_lo[..])}, one per
-// lane of a half warp (an 8-byte shared load is served per half warp, so lanes
-// l and l + 16 sharing a copy never conflict); entry stride 256 bytes. The
-// table is aligned to its own size, so the address of (entry, lane) is the
-// entry number OR-ed into bits 8.. of the lane's base: for 4-bit keys a single
-// byte permute of the key word.
+// Entry e (a key byte, or a 6-bit pair of 3-bit indices) holds 32 copies of
+// half2(c'[lo idx], c'[hi idx]), one per lane, so a warp's lookups never
+// conflict; c' = fp16(gamma * c), gamma the per-codebook scale chosen on the
+// host (the query is divided by it). Entry stride 256 bytes, of which the
+// copies fill 128. The table is aligned to its own size, so the address of
+// (entry, lane) is the entry number OR-ed into bits 8.. of the lane's base: for
+// 4-bit keys a single byte permute of the key word.
 template <int KMODE>
 __host__ __device__ constexpr uint32_t lut_bytes() { return KMODE == kMse4 ? 65536u : (KMODE == kMse3 ? 16384u : 0u); }
 
@@ -310,11 +314,9 @@ __device__ void build_lut(uint32_t lut, const float* cent, int tid, int nthreads
   constexpr int kEntries = KMODE == kMse4 ? 256 : 64;
   constexpr int kShift = KMODE == kMse4 ? 4 : 3;
   constexpr int kMask = (1 << kShift) - 1;
-  for (int i = tid; i < kEntries * 16; i += nthreads) {
-    const int e = i >> 4;
-    uint32_t hi, lo;
-    split_half2(cent[e & kMask], cent[(e >> kShift) & kMask], hi, lo);
-    sts64(lut + 256u * e + 8u * (i & 15), make_uint2(hi, lo));
+  for (int i = tid; i < kEntries * 32; i += nthreads) {
+    const int e = i >> 5;
+    sts32(lut + 256u * e + 4u * (i & 31), pack_half2(cent[e & kMask], cent[(e >> kShift) & kMask]));
   }
 }
 
@@ -624,7 +626,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
   const bool colv0 = hd0 < G, colv1 = hd0 + 1 < G;
   const bool colmask = GBIG ? G < 8 : G < 4;    // some columns carry no head
   uint32_t lut_lane = 0;
-  if constexpr (KMODE != kFp8) lut_lane = lut + 8u * (lane & 15);
+  if constexpr (KMODE != kFp8) lut_lane = lut + 4u * lane;
   uint32_t stg[kStages];
 #pragma unroll
   for (int s = 0; s < kStages; ++s) stg[s] = stage_at(first, lut, klut, a.stage_bytes, j * kStages + s);
@@ -772,38 +774,37 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
           kh[i] = make_uint4(lds32(rb), lds32(rb + 4), lds32(rb + 8), 0u);
         }
       }
-      // M rows: 8 tokens x {centroid hi part, centroid lo part}; k-step s holds
-      // this lane's coordinates 32c + 4s .. +3 (two key bytes = two LUT entries,
-      // each entry = the (hi, lo) operand pair of one row pair)
-      float Sg[kChunk][4], Sh[kChunk][4];
+      // M rows: tokens g and g + 8; k-step s holds this lane's coordinates
+      // 32c + 4s .. +3 (two key bytes = two LUT entries of two centroids each).
+      // Two accumulators per tile (even and odd k-steps; G > 4: hi and lo query
+      // parts) halve the dependent mma chains.
+      float va[kChunk][4], vb[kChunk][4];
 #pragma unroll
       for (int i = 0; i < kChunk; ++i)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) Sg[i][k] = Sh[i][k] = 0.f;
+        for (int k = 0; k < 4; ++k) va[i][k] = vb[i][k] = 0.f;
 #pragma unroll
       for (int s2 = 0; s2 < 8; ++s2) {
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
-          const uint2 g0 = lds64(lut_addr<KMODE>(kg[i], 2 * s2, lut_lane));
-          const uint2 g1 = lds64(lut_addr<KMODE>(kg[i], 2 * s2 + 1, lut_lane));
-          const uint2 h0 = lds64(lut_addr<KMODE>(kh[i], 2 * s2, lut_lane));
-          const uint2 h1 = lds64(lut_addr<KMODE>(kh[i], 2 * s2 + 1, lut_lane));
-          mma16816(Sg[i], g0.x, g0.y, g1.x, g1.y, qb[2 * s2], qb[2 * s2 + 1]);
-          mma16816(Sh[i], h0.x, h0.y, h1.x, h1.y, qb[2 * s2], qb[2 * s2 + 1]);
+          const uint32_t g0 = lds32(lut_addr<KMODE>(kg[i], 2 * s2, lut_lane));
+          const uint32_t g1 = lds32(lut_addr<KMODE>(kg[i], 2 * s2 + 1, lut_lane));
+          const uint32_t h0 = lds32(lut_addr<KMODE>(kh[i], 2 * s2, lut_lane));
+          const uint32_t h1 = lds32(lut_addr<KMODE>(kh[i], 2 * s2 + 1, lut_lane));
           if (GBIG) {
-            mma16816(Sg[i], g0.x, g0.y, g1.x, g1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
-            mma16816(Sh[i], h0.x, h0.y, h1.x, h1.y, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
+            mma16816(va[i], g0, h0, g1, h1, qb[2 * s2], qb[2 * s2 + 1]);
+            mma16816(vb[i], g0, h0, g1, h1, qb[16 + 2 * s2], qb[16 + 2 * s2 + 1]);
+          } else if ((s2 & 1) == 0) {
+            mma16816(va[i], g0, h0, g1, h1, qb[2 * s2], qb[2 * s2 + 1]);
+          } else {
+            mma16816(vb[i], g0, h0, g1, h1, qb[2 * s2], qb[2 * s2 + 1]);
           }
         }
       }
-      // rows g (hi part) + g + 8 (lo part) of each token: same lane
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        v[i][0] = Sg[i][0] + Sg[i][2];
-        v[i][1] = Sg[i][1] + Sg[i][3];
-        v[i][2] = Sh[i][0] + Sh[i][2];
-        v[i][3] = Sh[i][1] + Sh[i][3];
-      }
+      for (int i = 0; i < kChunk; ++i)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[i][k] = va[i][k] + vb[i][k];
     }
 
     // ---- scores: q hi + lo columns, norms, masks
@@ -1129,6 +1130,50 @@ int device_sms() {
   return sms;
 }
 
+// fp16 round-to-nearest-even of a double in the fp16 normal or subnormal range.
+double round_fp16(double x) {
+  if (x == 0.0) return 0.0;
+  int e = 0;
+  const double f = std::frexp(x, &e);   // x = f 2^e, 0.5 <= |f| < 1
+  if (e <= -14) return std::ldexp(std::nearbyint(std::ldexp(x, 24)), -24);   // subnormal: steps of 2^-24
+  return std::ldexp(std::nearbyint(std::ldexp(f, 11)), e - 11);              // 11 significant bits
+}
+
+// The decode holds the centroids c as fp16(gamma c) and divides the query by
+// gamma, so its scores carry only the rounding of gamma c. gamma is the step of
+// [1, 2) (2^-16 grid) whose largest relative rounding error over the nonzero
+// centroids is smallest: for the d = 128, 4-bit codebook about 9e-5 against
+// 3.5e-4 at gamma = 1. Memoised per codebook (the search takes a few ms).
+float centroid_scale(const float* c, int n) {
+  static std::mutex mu;
+  struct Memo { int n; float c[16]; float g; };
+  static Memo memo[8];
+  static int used = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int m = 0; m < used; ++m) {
+    bool same = memo[m].n == n;
+    for (int i = 0; same && i < n; ++i) same = memo[m].c[i] == c[i];
+    if (same) return memo[m].g;
+  }
+  double best_err = 1e300;
+  float best = 1.f;
+  for (int step = 0; step < 65536; ++step) {
+    const float g = 1.f + static_cast<float>(step) * (1.f / 65536.f);
+    double err = 0.0;
+    for (int i = 0; i < n && err < best_err; ++i) {
+      if (c[i] == 0.f) continue;
+      const double x = static_cast<double>(static_cast<float>(static_cast<double>(g) * c[i]));
+      err = std::fmax(err, std::fabs(round_fp16(x) - static_cast<double>(g) * c[i]) / std::fabs(static_cast<double>(g) * c[i]));
+    }
+    if (err < best_err) { best_err = err; best = g; }
+  }
+  Memo& slot = memo[used < 8 ? used++ : 7];
+  slot.n = n;
+  for (int i = 0; i < 16; ++i) slot.c[i] = i < n ? c[i] : 0.f;
+  slot.g = best;
+  return best;
+}
+
 // Host-side checks and sizes shared by both stages (no CUDA call unless
 // query_device; the workspace size never depends on the device).
 tq_status make_plan(const tq_config* cfg, int batch, int max_seq_len, int bt_stride, bool query_device,
@@ -1286,7 +1331,10 @@ tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* 
   a.dyn_bytes = 0;
   const float sm_scale = scale > 0.f ? scale : 0.088388347648318440f;   // 1/sqrt(128)
   a.qscale = sm_scale * 1.4426950408889634f;                              // log2(e)
-  for (int i = 0; i < 16; ++i) a.cent[i] = (!P.L.key_fp8 && i < cb->num_levels) ? cb->centroids[i] : 0.f;
+  const float gamma = P.L.key_fp8 ? 1.f : centroid_scale(cb->centroids, cb->num_levels);
+  a.qscale /= gamma;
+  for (int i = 0; i < 16; ++i)
+    a.cent[i] = (!P.L.key_fp8 && i < cb->num_levels) ? static_cast<float>(static_cast<double>(gamma) * cb->centroids[i]) : 0.f;
 
   cudaError_t err;
   if (P.L.key_fp8) err = launch_split<kFp8>(a, q_dtype, stream, P.sms);

@@ -93,6 +93,16 @@ def test_decode_partition_invariance(tq, pt):
     assert_decode_close(got, ref, torch.float32)
 
 
+# The reduce has two launch shapes: a CTA per query head when there are few
+# (sequence, KV head) pairs (every small workload above), a CTA per pair when
+# they outnumber half the SMs (40 x 8 = 320 pairs here).
+@pytest.mark.parametrize("pt", [None, 0])
+def test_decode_many_pairs(tq, pt):
+    w, inp, oc, q, ref = oracle_case("k3v4_small", batch=40)
+    got = gpu_decode(tq, w, inp, oc.cache, partition_tokens=pt)
+    assert_decode_close(got, ref, torch.float32)
+
+
 @pytest.mark.parametrize("bs", [32, 64, 128])
 def test_decode_block_sizes(tq, bs):
     w, inp, oc, q, ref = oracle_case("gqa_small", block_size=bs)

@@ -154,6 +154,7 @@ struct ReduceArgs {
   const float* rec_lse;
   void* out;
   int batch, n_q, n_kv, group, part_tiles, num_parts, max_seq_len, cap, num_warps;
+  int early_lens;   // launched right after the split kernel of the same decode
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -988,130 +989,303 @@ __device__ __forceinline__ int reduce_len(const ReduceArgs& a, int b) {
   return min(max(__ldg(a.seq_lens + b), 0), min(a.max_seq_len, a.cap));
 }
 
-// One CTA per (sequence, KV head); thread (gg, d) = query head gg of the
-// group, coordinate d. The records of a segment are those of the consumer
-// warps whose ranges overlap it, a contiguous warp range. Warp 0 computes
-// that range (the only divisions), then walks it 32 warps at a time, one
-// candidate per lane: whether the warp owns a tile at all, its record, and
-// the record's LSE for every head; it publishes merge weights per (candidate,
-// head). Every thread then adds its coordinate of the weighted partials
-// (record 0 stands in for a warp whose range is empty, and a select, not a
-// multiply, drops it: the workspace may hold any bits). Chunks of candidates
-// and partitions are merged online.
+// The reduce. The records of a partition are those of the consumer warps
+// whose ranges overlap it, a contiguous warp range; a (partition, warp)
+// candidate whose warp owns no tile at all has no record. Record 0 stands in
+// for such a candidate, and a select, not a multiply, drops it (the workspace
+// may hold any bits). All index work depends on seq_lens only. When the launch
+// directly follows the split kernel of the same decode (early_lens), that work
+// runs before the dependency wait, which comes right before the first load of
+// a record: the split kernel triggers this launch only after its own wait, so
+// every earlier kernel has completed, and it writes no lengths.
+__device__ __forceinline__ long long div_nw(long long x, long long y, bool narrow) {
+  return narrow ? static_cast<long long>(static_cast<unsigned>(x) / static_cast<unsigned>(y)) : x / y;
+}
+
+// Warp-wide: tiles before sequence b and in total (x n_kv) into pre[0..1]; the
+// length of b into *len.
+__device__ __forceinline__ void reduce_prefix(const ReduceArgs& a, int b, int lane, long long* pre, int* len) {
+  long long before = 0, total = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    const int j = b0 + lane;
+    const int len_j = j < a.batch ? reduce_len(a, j) : 0;
+    if (j == b) *len = len_j;
+    long long nt = (len_j + kTileTokens - 1) / kTileTokens;
+    long long nb = j < b ? nt : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      nt += __shfl_xor_sync(0xffffffffu, nt, o);
+      nb += __shfl_xor_sync(0xffffffffu, nb, o);
+    }
+    total += nt;
+    before += nb;
+  }
+  if (lane == 0) {
+    pre[0] = before * a.n_kv;
+    pre[1] = total * a.n_kv;
+  }
+}
+
+// Warp-wide, lane = partition p (p >= parts: none): the first consumer warp
+// whose range overlaps partition p (tiles [seq0 + p ppt, seq0 + min((p + 1)
+// ppt, nt)) of a line of T tiles split over nw warps) into *wf; returns the
+// inclusive scan over the lanes of the overlapping warp counts.
+__device__ __forceinline__ int partition_scan(int p, int parts, long long seq0, int ppt, int nt, long long T,
+                                              long long nw, bool narrow, int lane, long long* wf) {
+  *wf = 0;
+  int inc = 0;
+  if (p < parts) {
+    const long long t0 = seq0 + static_cast<long long>(p) * ppt;
+    const long long t1 = seq0 + min(static_cast<long long>(p + 1) * ppt, static_cast<long long>(nt));
+    *wf = div_nw((t0 + 1) * nw - 1, T, narrow);
+    inc = static_cast<int>(div_nw(t1 * nw - 1, T, narrow) - *wf + 1);
+  }
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  return inc;
+}
+
+// Warp w owns tiles [T w / nw, T (w + 1) / nw): does it own any?
+__device__ __forceinline__ bool warp_owns_tiles(long long w, long long T, long long nw, bool narrow) {
+  return div_nw(T * w, nw, narrow) != div_nw(T * (w + 1), nw, narrow);
+}
+
+// Many (sequence, KV head) pairs with few partials each: one CTA per pair,
+// thread (gg, d) = query head gg of the group, coordinate d. Warp 0 computes
+// the warp ranges of 32 partitions at a time and a scan of their sizes, then
+// takes the (partition, warp) candidates 16 at a time, one per lane, and
+// publishes their records. Every thread then loads its coordinate of all their
+// partials while warp 0 loads their LSEs for every head and publishes merge
+// weights per (candidate, head), so the two loads overlap. Chunks are merged
+// online.
 template <typename TO>
-__global__ void __launch_bounds__(8 * kD) reduce_kernel(const ReduceArgs a) {
+__global__ void __launch_bounds__(8 * kD) reduce_bh_kernel(const ReduceArgs a) {
+  constexpr int kCand = 16;
   __shared__ long long s_pre[2];
-  __shared__ long long s_wf[32], s_wl[32], s_q[32], s_r[32];
-  __shared__ int s_len;
-  __shared__ int s_rec[32];
-  __shared__ float s_w[32][8];
+  __shared__ long long s_wf[32];
+  __shared__ int s_inc[32];
+  __shared__ int s_len, s_cnt;
+  __shared__ int s_rec[kCand];
+  __shared__ float s_w[kCand][8];
   __shared__ float s_alpha[8];
-  __shared__ int s_cnt;
   const int h = blockIdx.x, b = blockIdx.y;
   const int G = a.group;
   const int gg = threadIdx.x / kD, d = threadIdx.x - gg * kD;
   const int lane = threadIdx.x & 31;
   const bool w0 = threadIdx.x < 32;
-  grid_dep_wait();   // records (and everything else) come from earlier kernels
-  grid_dep_launch();
-  if (w0) {   // tiles before sequence b, and in total; the length of b
-    long long before = 0, total = 0;
-    for (int b0 = 0; b0 < a.batch; b0 += 32) {
-      const int j = b0 + lane;
-      const int len_j = j < a.batch ? reduce_len(a, j) : 0;
-      if (j == b) s_len = len_j;
-      long long nt = (len_j + kTileTokens - 1) / kTileTokens;
-      long long nb = j < b ? nt : 0;
-      for (int o = 1; o < 32; o <<= 1) {
-        nt += __shfl_xor_sync(0xffffffffu, nt, o);
-        nb += __shfl_xor_sync(0xffffffffu, nb, o);
-      }
-      total += nt;
-      before += nb;
+  bool waited = false;
+  auto wait_once = [&]() {   // every global access but the lengths comes after it
+    if (!waited) {
+      grid_dep_wait();
+      grid_dep_launch();
+      waited = true;
     }
-    if (lane == 0) { s_pre[0] = before * a.n_kv; s_pre[1] = total * a.n_kv; }
-  }
+  };
+  if (!a.early_lens) wait_once();
+  if (w0) reduce_prefix(a, b, lane, s_pre, &s_len);
   __syncthreads();
   const long long orow = static_cast<long long>(b) * a.n_q + static_cast<long long>(h) * G + gg;
   const int len = s_len;
-  if (len <= 0) { store_out<TO>(a.out, orow * kD + d, 0.f); return; }
+  if (len <= 0) {
+    wait_once();
+    store_out<TO>(a.out, orow * kD + d, 0.f);
+    return;
+  }
   const int nt = (len + kTileTokens - 1) / kTileTokens;
   const long long T = s_pre[1], nw = a.num_warps;
+  const bool narrow = (T + 1) * nw < (1ll << 32);
   const long long seq0 = s_pre[0] + static_cast<long long>(h) * nt;   // first tile of (b, h)
+  const long long seg0 = (static_cast<long long>(b) * a.n_kv + h) * a.num_parts;
   const int ppt = a.part_tiles > 0 ? a.part_tiles : nt;
   const int parts = (nt + ppt - 1) / ppt;
-  long long Tq = 0, Tr = 0;   // warp w owns tiles [T w / nw, T (w + 1) / nw); T = Tq nw + Tr
-  if (w0) {
-    Tq = T / nw;
-    Tr = T - Tq * nw;
-  }
   float acc = 0.f, den = 0.f;
   float mxh[8];   // warp 0: running LSE max per head
 #pragma unroll
   for (int k = 0; k < 8; ++k) mxh[k] = -INFINITY;
   for (int p0 = 0; p0 < parts; p0 += 32) {
-    if (w0 && p0 + lane < parts) {   // contributing warps of partition p0 + lane
-      const int p = p0 + lane;
-      const long long t0 = seq0 + static_cast<long long>(p) * ppt;
-      const long long t1 = seq0 + min(static_cast<long long>(p + 1) * ppt, static_cast<long long>(nt));
-      const long long wf = ((t0 + 1) * nw - 1) / T, wl = (t1 * nw - 1) / T;
-      const long long q = T * wf / nw;
+    if (w0) {
+      long long wf;
+      const int inc = partition_scan(p0 + lane, parts, seq0, ppt, nt, T, nw, narrow, lane, &wf);
       s_wf[lane] = wf;
-      s_wl[lane] = wl;
-      s_q[lane] = q;
-      s_r[lane] = T * wf - q * nw;
+      s_inc[lane] = inc;
     }
     __syncthreads();
-    const int pend = min(parts - p0, 32);
-    for (int pi = 0; pi < pend; ++pi) {
-      const long long seg = (static_cast<long long>(b) * a.n_kv + h) * a.num_parts + p0 + pi;
-      const long long wf = s_wf[pi], wl = s_wl[pi];
-      long long q0 = s_q[pi], r0 = s_r[pi];   // first tile of warp wb, and remainder
-      for (long long wb = wf; wb <= wl; wb += 32) {
-        if (w0) {
-          // candidate wb + lane starts at tile q0 + lane Tq + floor((r0 + lane Tr) / nw)
-          const long long i = lane;
-          const long long rr = r0 + i * Tr, rn = rr + Tr;
-          const long long qi = q0 + i * Tq + rr / nw;
-          const long long qn = q0 + (i + 1) * Tq + rn / nw;
-          const bool ok = wb + i <= wl && qn != qi;   // warp wb + i owns at least one tile
-          const long long rec = seg + wb + i;
-          s_rec[lane] = ok ? static_cast<int>(rec) : 0;
-          if (lane == 0) s_cnt = static_cast<int>(min(32ll, wl - wb + 1));
+    const int C = s_inc[31];   // candidates (partition, warp) of the group, partition-major
+    for (int k0 = 0; k0 < C; k0 += kCand) {
+      bool ok = false;
+      long long rec = 0;
+      if (w0) {
+        const int k = k0 + lane;
+        int pi = 0;   // partition of candidate k: the first with inclusive count > k
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            if (k < G) {
-              const float lse = ok ? a.rec_lse[rec * G + k] : -INFINITY;
-              float cm = lse;
-              for (int o = 1; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-              const float nm = fmaxf(mxh[k], cm);
-              s_w[lane][k] = lse == -INFINITY ? 0.f : exp2f(lse - nm);
-              if (lane == 0) s_alpha[k] = mxh[k] == -INFINITY ? 0.f : exp2f(mxh[k] - nm);
-              mxh[k] = nm;
-            }
+        for (int step = 16; step >= 1; step >>= 1)
+          if (s_inc[pi + step - 1] <= k) pi += step;
+        const long long w = s_wf[pi] + (k - (pi > 0 ? s_inc[pi - 1] : 0));
+        ok = lane < kCand && k < C && warp_owns_tiles(w, T, nw, narrow);
+        rec = seg0 + p0 + pi + w;
+        if (lane < kCand) s_rec[lane] = ok ? static_cast<int>(rec) : 0;
+        if (lane == 0) s_cnt = min(kCand, C - k0);
+      }
+      __syncthreads();   // candidates published
+      wait_once();
+      const int cnt = s_cnt;
+      float x[kCand];    // this thread's coordinate of every candidate's partial
+#pragma unroll
+      for (int i = 0; i < kCand; ++i)
+        x[i] = i < cnt ? a.rec_o[(static_cast<long long>(s_rec[i]) * G + gg) * kD + d] : 0.f;
+      if (w0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (k < G) {
+            const float lse = ok ? a.rec_lse[rec * G + k] : -INFINITY;
+            float cm = lse;
+            for (int o = 1; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+            const float nm = fmaxf(mxh[k], cm);
+            if (lane < kCand) s_w[lane][k] = lse == -INFINITY ? 0.f : exp2f(lse - nm);
+            if (lane == 0) s_alpha[k] = mxh[k] == -INFINITY ? 0.f : exp2f(mxh[k] - nm);
+            mxh[k] = nm;
           }
-          const long long r32 = r0 + 32 * Tr;   // the next 32 candidates
-          q0 += 32 * Tq + r32 / nw;
-          r0 = r32 % nw;
         }
-        __syncthreads();
-        const int cnt = s_cnt;
-        const float al = s_alpha[gg];
-        acc *= al;
-        den *= al;
-#pragma unroll 4
-        for (int i = 0; i < cnt; ++i) {
+      }
+      __syncthreads();   // weights published
+      const float al = s_alpha[gg];
+      acc *= al;
+      den *= al;
+#pragma unroll
+      for (int i = 0; i < kCand; ++i) {
+        if (i < cnt) {
           const float wgt = s_w[i][gg];
-          const float x = a.rec_o[(static_cast<long long>(s_rec[i]) * G + gg) * kD + d];
           den += wgt;
-          acc = wgt != 0.f ? fmaf(wgt, x, acc) : acc;
+          acc = wgt != 0.f ? fmaf(wgt, x[i], acc) : acc;
         }
-        __syncthreads();   // weights used before warp 0 writes the next chunk's
+      }
+      __syncthreads();   // weights and candidates used before warp 0 writes the next chunk's
+    }
+    __syncthreads();     // the group's scan is read before warp 0 writes the next
+  }
+  wait_once();
+  store_out<TO>(a.out, orow * kD + d, den > 0.f ? acc / den : 0.f);
+}
+
+// Few pairs with many partials each: one CTA per (sequence, query head), 4
+// warps; thread d of 128 = coordinate d in the final merge. Every warp scans
+// the partitions 32 at a time; the (partition, warp) candidates of a group,
+// partition-major, form chunks of 32 that go round robin to the 4 warps, one
+// candidate per lane. A warp loads the records of its chunk (16 bytes per lane
+// per record) before their weights are known, together with the candidates'
+// LSEs, and merges online; the 4 warps' states are merged at the end.
+constexpr int kReduceThreads = 128;
+
+template <typename TO>
+__global__ void __launch_bounds__(kReduceThreads) reduce_qh_kernel(const ReduceArgs a) {
+  __shared__ long long s_pre[2];
+  __shared__ int s_len;
+  __shared__ float s_m[4], s_den[4];
+  __shared__ __align__(16) float s_acc[4][kD];
+  const int G = a.group;
+  const int h = blockIdx.x / G, gg = blockIdx.x - h * G, b = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  bool waited = false;
+  auto wait_once = [&]() {   // every global access but the lengths comes after it
+    if (!waited) {
+      grid_dep_wait();
+      grid_dep_launch();
+      waited = true;
+    }
+  };
+  if (!a.early_lens) wait_once();
+  if (warp == 0) reduce_prefix(a, b, lane, s_pre, &s_len);
+  __syncthreads();
+  const long long orow = static_cast<long long>(b) * a.n_q + static_cast<long long>(h) * G + gg;
+  const int len = s_len;
+  if (len <= 0) {
+    wait_once();
+    store_out<TO>(a.out, orow * kD + threadIdx.x, 0.f);
+    return;
+  }
+  const int nt = (len + kTileTokens - 1) / kTileTokens;
+  const long long T = s_pre[1], nw = a.num_warps;
+  const bool narrow = (T + 1) * nw < (1ll << 32);
+  const long long seq0 = s_pre[0] + static_cast<long long>(h) * nt;   // first tile of (b, h)
+  const long long seg0 = (static_cast<long long>(b) * a.n_kv + h) * a.num_parts;
+  const int ppt = a.part_tiles > 0 ? a.part_tiles : nt;
+  const int parts = (nt + ppt - 1) / ppt;
+  const float4* rec_o = reinterpret_cast<const float4*>(a.rec_o);
+  float m = -INFINITY, den = 0.f;   // den: this lane's share of the sum of weights
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int chunk = 0;                    // chunk number over all groups
+  for (int p0 = 0; p0 < parts; p0 += 32) {
+    long long wf;
+    const int inc = partition_scan(p0 + lane, parts, seq0, ppt, nt, T, nw, narrow, lane, &wf);
+    const int C = __shfl_sync(0xffffffffu, inc, 31);   // candidates of the group
+    for (int k0 = 0; k0 < C; k0 += 32, ++chunk) {
+      if ((chunk & 3) != warp) continue;
+      const int k = k0 + lane;
+      int pi = 0;   // partition of candidate k: the first with inclusive count > k
+#pragma unroll
+      for (int step = 16; step >= 1; step >>= 1)
+        if (__shfl_sync(0xffffffffu, inc, pi + step - 1) <= k) pi += step;
+      const long long wfp = __shfl_sync(0xffffffffu, wf, pi);
+      const int excl = __shfl_sync(0xffffffffu, inc, pi > 0 ? pi - 1 : 0);
+      const long long w = wfp + (k - (pi > 0 ? excl : 0));
+      const bool ok = k < C && warp_owns_tiles(w, T, nw, narrow);
+      const int rec = ok ? static_cast<int>(seg0 + p0 + pi + w) : 0;
+      wait_once();
+      const float lse = ok ? __ldg(a.rec_lse + static_cast<long long>(rec) * G + gg) : -INFINITY;
+      const int n = min(32, C - k0);
+      float4 x[16];   // records of candidates 0..15, loaded before the weights are known
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int r = __shfl_sync(0xffffffffu, rec, i);
+        x[i] = i < n ? __ldg(rec_o + (static_cast<long long>(r) * G + gg) * (kD / 4) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float cm = lse;
+      for (int o = 1; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+      const float nm = fmaxf(m, cm);
+      const float al = m == -INFINITY ? 0.f : exp2f(m - nm);
+      m = nm;
+      den *= al;
+      acc.x *= al; acc.y *= al; acc.z *= al; acc.w *= al;
+      const float wl = lse == -INFINITY ? 0.f : exp2f(lse - nm);
+      den += wl;
+      auto add = [&](float wg, const float4& v) {
+        acc.x = wg != 0.f ? fmaf(wg, v.x, acc.x) : acc.x;
+        acc.y = wg != 0.f ? fmaf(wg, v.y, acc.y) : acc.y;
+        acc.z = wg != 0.f ? fmaf(wg, v.z, acc.z) : acc.z;
+        acc.w = wg != 0.f ? fmaf(wg, v.w, acc.w) : acc.w;
+      };
+#pragma unroll
+      for (int i = 0; i < 16; ++i) add(__shfl_sync(0xffffffffu, wl, i), x[i]);
+      if (n > 16) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = __shfl_sync(0xffffffffu, rec, 16 + i);
+          x[i] = 16 + i < n ? __ldg(rec_o + (static_cast<long long>(r) * G + gg) * (kD / 4) + lane)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) add(__shfl_sync(0xffffffffu, wl, 16 + i), x[i]);
       }
     }
-    __syncthreads();   // this group's ranges are used before warp 0 writes the next
   }
-  store_out<TO>(a.out, orow * kD + d, den > 0.f ? acc / den : 0.f);
+  wait_once();
+  for (int o = 1; o < 32; o <<= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if (lane == 0) { s_m[warp] = m; s_den[warp] = den; }
+  *reinterpret_cast<float4*>(&s_acc[warp][4 * lane]) = acc;
+  __syncthreads();
+  float M = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) M = fmaxf(M, s_m[u]);
+  float num = 0.f, dsum = 0.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float f = s_m[u] == -INFINITY ? 0.f : exp2f(s_m[u] - M);
+    num = fmaf(f, s_acc[u][threadIdx.x], num);
+    dsum = fmaf(f, s_den[u], dsum);
+  }
+  store_out<TO>(a.out, orow * kD + threadIdx.x, dsum > 0.f ? num / dsum : 0.f);
 }
 
 // ---------------------------------------------------------------- host glue
@@ -1344,7 +1518,8 @@ tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* 
 }
 
 tq_status run_reduce(const tq_config* cfg, const int* seq_lens, int batch, int max_seq_len, int bt_stride,
-                     void* out, int out_dtype, const void* workspace, size_t ws_bytes, cudaStream_t stream) {
+                     void* out, int out_dtype, const void* workspace, size_t ws_bytes, cudaStream_t stream,
+                     bool after_split) {
   if (bt_stride < 1) return TQ_ERR_INVALID_ARG;
   Plan P;
   tq_status st = make_plan(cfg, batch, max_seq_len, bt_stride, false, &P);
@@ -1374,12 +1549,22 @@ tq_status run_reduce(const tq_config* cfg, const int* seq_lens, int batch, int m
   r.max_seq_len = max_seq_len;
   r.cap = P.cap;
   r.num_warps = P.sms * warps;
-  const dim3 grid(static_cast<unsigned>(cfg->num_kv_heads), static_cast<unsigned>(batch));
+  r.early_lens = after_split ? 1 : 0;
   cudaError_t err;
-  const dim3 block(static_cast<unsigned>(G * kD));
-  if (out_dtype == TQ_DTYPE_F32) err = launch_pdl(reduce_kernel<float>, grid, block, 0, stream, r);
-  else if (out_dtype == TQ_DTYPE_F16) err = launch_pdl(reduce_kernel<__half>, grid, block, 0, stream, r);
-  else err = launch_pdl(reduce_kernel<__nv_bfloat16>, grid, block, 0, stream, r);
+  if (static_cast<long long>(batch) * cfg->num_kv_heads * 2 <= P.sms) {
+    // few (sequence, KV head) pairs, many partials each: a CTA per query head
+    const dim3 grid(static_cast<unsigned>(cfg->num_q_heads), static_cast<unsigned>(batch));
+    const dim3 block(static_cast<unsigned>(kReduceThreads));
+    if (out_dtype == TQ_DTYPE_F32) err = launch_pdl(reduce_qh_kernel<float>, grid, block, 0, stream, r);
+    else if (out_dtype == TQ_DTYPE_F16) err = launch_pdl(reduce_qh_kernel<__half>, grid, block, 0, stream, r);
+    else err = launch_pdl(reduce_qh_kernel<__nv_bfloat16>, grid, block, 0, stream, r);
+  } else {
+    const dim3 grid(static_cast<unsigned>(cfg->num_kv_heads), static_cast<unsigned>(batch));
+    const dim3 block(static_cast<unsigned>(G * kD));
+    if (out_dtype == TQ_DTYPE_F32) err = launch_pdl(reduce_bh_kernel<float>, grid, block, 0, stream, r);
+    else if (out_dtype == TQ_DTYPE_F16) err = launch_pdl(reduce_bh_kernel<__half>, grid, block, 0, stream, r);
+    else err = launch_pdl(reduce_bh_kernel<__nv_bfloat16>, grid, block, 0, stream, r);
+  }
   return err == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 
@@ -1407,7 +1592,7 @@ tq_status tq_decode_reduce(const tq_config* cfg, const int* seq_lens, int batch,
                            void* out, int out_dtype, const void* workspace, size_t workspace_bytes,
                            tq_stream_t stream) {
   return tq::run_reduce(cfg, seq_lens, batch, max_seq_len, bt_stride, out, out_dtype, workspace,
-                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+                        workspace_bytes, reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 tq_status tq_decode(const tq_config* cfg, const tq_codebook* cb, const void* q, int q_dtype, const void* cache,
@@ -1423,7 +1608,7 @@ tq_status tq_decode(const tq_config* cfg, const tq_codebook* cb, const void* q, 
                                   batch, max_seq_len, scale, workspace, workspace_bytes, dev_status, s);
   if (st != TQ_OK) return st;
   return tq::run_reduce(cfg, seq_lens, batch, max_seq_len, bt_stride, out, out_dtype, workspace,
-                        workspace_bytes, s);
+                        workspace_bytes, s, true);
 }
 
 }  // extern "C"

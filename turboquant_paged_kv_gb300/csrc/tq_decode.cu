@@ -643,7 +643,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
 #pragma unroll
     for (int e = 0; e < 2; ++e)
 #pragma unroll
-      for (int o_ = 4; o_ < 32; o_ <<= 1) {
+      for (int o_ = GBIG ? 4 : 2; o_ < 32; o_ <<= 1) {   // G <= 4: lanes c, c ^ 2 hold tokens g, g + 8
         l_[e] += __shfl_xor_sync(0xffffffffu, l_[e], o_);
         z_[e] += __shfl_xor_sync(0xffffffffu, z_[e], o_);
       }
@@ -808,7 +808,83 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
         for (int k = 0; k < 4; ++k) v[i][k] = va[i][k] + vb[i][k];
     }
 
-    // ---- scores: q hi + lo columns, norms, masks
+    // ---- scores, probabilities and O^T += V^T . P^T
+    if constexpr (!GBIG) {
+      // G <= 4: after the hi/lo exchange lanes c and c ^ 2 hold the same
+      // scores; lane c < 2 carries on with token g, lane c >= 2 with token
+      // g + 8 (its l, z are summed over the pair at the end), and one more
+      // exchange gives each lane the other half of the P^T operands.
+      const int tk = lo_lane ? g + 8 : g;
+      float t0[kChunk], t1[kChunk], sv[kChunk], sz[kChunk];
+      float cm0 = -INFINITY, cm1 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        const uint32_t tb = st + i * a.tile_bytes;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[i][k] += __shfl_xor_sync(0xffffffffu, v[i][k], 2);
+        float x0 = lo_lane ? v[i][2] : v[i][0], x1 = lo_lane ? v[i][3] : v[i][1];
+        if constexpr (KMODE != kFp8) {
+          const float nk = lds_h2f(tb + a.knorm_off + 2 * tk);
+          x0 *= nk;
+          x1 *= nk;
+        }
+        sv[i] = lds_h2f(tb + a.vscale_off + 2 * tk);
+        sz[i] = lds_h2f(tb + a.vzero_off + 2 * tk);
+        if (tk >= nv[i]) { x0 = x1 = -INFINITY; sv[i] = 0.f; sz[i] = 0.f; }   // missing, ragged, past the end
+        if (colmask) {
+          if (!colv0) x0 = -INFINITY;
+          if (!colv1) x1 = -INFINITY;
+        }
+        t0[i] = x0;
+        t1[i] = x1;
+        cm0 = fmaxf(cm0, x0);
+        cm1 = fmaxf(cm1, x1);
+      }
+      if (__any_sync(0xffffffffu, cm0 > m0 + kTau || cm1 > m1 + kTau)) {   // rare: move the max, rescale
+#pragma unroll
+        for (int o_ = 2; o_ < 32; o_ <<= 1) {
+          cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, o_));
+          cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, o_));
+        }
+        float al0 = 1.f, al1 = 1.f;
+        if (cm0 > m0 + kTau) { al0 = ex2(m0 - cm0); m0 = cm0; }
+        if (cm1 > m1 + kTau) { al1 = ex2(m1 - cm1); m1 = cm1; }
+        l0 *= al0; z0 *= al0; l1 *= al1; z1 *= al1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][0] *= al0; o[mt][2] *= al0;
+          o[mt][1] *= al1; o[mt][3] *= al1;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        const float p0 = ex2(t0[i] - m0), p1 = ex2(t1[i] - m1);
+        l0 += p0;
+        l1 += p1;
+        z0 = fmaf(p0, sz[i], z0);
+        z1 = fmaf(p1, sz[i], z1);
+        uint32_t hi, lo;   // hi/lo half2 of (col 2c, col 2c+1) for token tk
+        split_half2(p0 * sv[i], p1 * sv[i], hi, lo);
+        // b0 (tokens 0..7): hi parts from lanes c < 2, lo parts from c >= 2;
+        // b1 (tokens 8..15) the same: each lane lacks one of the two
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, lo_lane ? hi : lo, 2);
+        const uint32_t b0 = movmatrix_trans(lo_lane ? recv : hi), b1 = movmatrix_trans(lo_lane ? lo : recv);
+        const uint32_t vt = st + i * a.tile_bytes + a.v_off + 16 * (g ^ (2 * c));
+        const uint4 va = lds128(vt + 128 * c);         // tokens 2c, 2c+1
+        const uint4 vb = lds128(vt + 128 * (c + 4));   // tokens 2c+8, 2c+9
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t wa = word_of(va, k), wb = word_of(vb, k);
+          const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+          mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0, b1);
+          mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0,
+                   b1);
+        }
+      }
+      return;
+    }
+
+    // ---- G > 4: every lane carries both of its tokens
     float svg[kChunk], svh[kChunk], szg[kChunk], szh[kChunk];
     float cm0 = -INFINITY, cm1 = -INFINITY;
 #pragma unroll

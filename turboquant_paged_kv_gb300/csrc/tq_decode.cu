@@ -527,6 +527,10 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
   if (mine && rem > 0) plan();
 
   const uint64_t policy = evict_first_policy();
+  const long long blk_bytes = static_cast<long long>(a.n_kv) * a.tiles_per_block * a.tile_bytes;   // one cache block
+  // stage_at without its division: stages [0, nb_front) lie before the LUT
+  const uint32_t nb_front = klut && lut > first ? (lut - first) / a.stage_bytes : (klut ? 0u : 0xFFFFFFFFu);
+  const uint32_t back = lut + klut;
   const uint32_t qslot = qslots + static_cast<uint32_t>(mine ? lane : 0) * a.qbuf_bytes;
   const uint32_t qbar = q_empty_bar(bars, W, mine ? lane : 0);
   uint32_t eparity = (1u << kStages) - 1;   // empty-barrier parity to wait for, per stage
@@ -551,7 +555,8 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
       const uint32_t fb = full_bar(bars, lane, ps);
       if (!mbar_test(fb + 8, (eparity >> ps) & 1u)) break;
       eparity ^= 1u << ps;
-      const uint32_t sa = stage_at(first, lut, klut, a.stage_bytes, lane * kStages + ps);
+      const uint32_t idx = static_cast<uint32_t>(lane * kStages + ps);
+      const uint32_t sa = idx < nb_front ? first + idx * a.stage_bytes : back + (idx - nb_front) * a.stage_bytes;
       const bool last = rem <= 0;
       uint32_t okm = 0, bytes = 0;
 #pragma unroll
@@ -570,9 +575,9 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
 #pragma unroll
       for (int i = 0; i < kChunk; ++i)
         if ((okm >> i) & 1u) {
-          const uint8_t* src = a.cache + ((static_cast<long long>(n_blk[i]) * a.n_kv + n_h) * a.tiles_per_block +
-                                          ((n_t + i) & (a.tiles_per_block - 1))) *
-                                             static_cast<long long>(a.tile_bytes);
+          const uint8_t* src = a.cache + static_cast<long long>(n_blk[i]) * blk_bytes +
+                               static_cast<uint32_t>(n_h * a.tiles_per_block + ((n_t + i) & (a.tiles_per_block - 1))) *
+                                   static_cast<uint32_t>(a.tile_bytes);
           bulk_g2s(sa + i * a.tile_bytes, src, a.tile_bytes, fb, policy);
         }
       if (newq) {

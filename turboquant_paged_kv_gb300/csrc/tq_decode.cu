@@ -241,7 +241,6 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
   return p;
 }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -570,7 +569,10 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
                                          static_cast<uint32_t>(n_len),
                                          static_cast<uint32_t>(n_n) | (okm << 4) | (last ? 256u : 0u) |
                                              (newq ? 512u : 0u)));
-      fence_proxy_async();
+      // No proxy fence: the consumer's reads of the stage are ordered before
+      // these copies by its arrive on the empty barrier (release) and the
+      // test above (acquire); the descriptor goes generic store -> generic load
+      // through the full barrier.
       mbar_expect(fb, bytes);
 #pragma unroll
       for (int i = 0; i < kChunk; ++i)

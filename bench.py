@@ -225,7 +225,11 @@ def run_tq(args):
 
     w = rank_workload(rank)
     inp = workloads.make_inputs(w, device=dev)
-    cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size, partition_tokens=args.partition)
+    # seq_lens and the block table are written long before each decode (the
+    # kernel right before it is tq_store), so the split kernel may plan before
+    # waiting for that kernel
+    cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size, partition_tokens=args.partition,
+                         flags=tq.TQ_FLAG_INDICES_READY)
     cb = tq.tq_build_codebook(w.d, 4)
     lay = tq.tq_layout_for(cfg)
     n_copies = 3

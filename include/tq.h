@@ -81,7 +81,20 @@ typedef struct {
                             one KV head; > 0 (a multiple of 16): partials are
                             also cut every partition_tokens positions. Work is
                             split evenly over the GPU in either case.          */
+  int flags;             /* OR of TQ_FLAG_* (0: none; unknown bits are an
+                            error, TQ_ERR_INVALID_ARG)                         */
 } tq_config;
+
+/* tq_config.flags. TQ_FLAG_INDICES_READY: the caller guarantees that the
+ * kernel launched immediately before tq_decode / tq_decode_partials on the
+ * same stream writes neither seq_lens nor block_table (for example: they were
+ * copied from the host earlier, and that kernel is tq_store or a projection).
+ * The split kernel then reads them, and plans its work, before it waits for
+ * that kernel (programmatic dependent launch), so the start-up chain lengths
+ * -> block ids overlaps the previous kernel's tail. It still waits before it
+ * reads q or the cache and before it writes anything. Breaking the guarantee
+ * gives results computed from stale indices; no fault. */
+#define TQ_FLAG_INDICES_READY 1
 
 /* Byte layout of the paged cache (this library's ABI).
  *

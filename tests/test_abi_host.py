@@ -75,7 +75,9 @@ def test_unsupported_shapes(tq):
     for cfg, want in [(tq.make_config("4bit_nc", 8, 8, head_dim=96), _abi.TQ_ERR_UNSUPPORTED),
                       (tq.make_config("4bit_nc", 8, 8, block_size=8), _abi.TQ_ERR_UNSUPPORTED),
                       (tq.make_config(17, 8, 8), _abi.TQ_ERR_INVALID_ARG),
-                      (tq.make_config("3bit_nc", 8, 8), _abi.TQ_ERR_UNSUPPORTED)]:
+                      (tq.make_config("3bit_nc", 8, 8), _abi.TQ_ERR_UNSUPPORTED),
+                      (tq.make_config("4bit_nc", 8, 8, flags=2), _abi.TQ_ERR_INVALID_ARG),
+                      (tq.make_config("4bit_nc", 8, 8, flags=tq.TQ_FLAG_INDICES_READY), _abi.TQ_OK)]:
         assert lib.tq_layout_for(ctypes.byref(cfg), ctypes.byref(lay)) == want
 
 

@@ -39,9 +39,10 @@ def oracle_case(name, **over):
 
 
 def gpu_decode(tq, w, inp, cache_np, out_dtype=torch.float32, partition_tokens=None, seq_lens=None,
-               block_table=None, q=None, status=None, max_seq_len=None):
+               block_table=None, q=None, status=None, max_seq_len=None, flags=0):
     cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size,
-                         partition_tokens=w.partition_tokens if partition_tokens is None else partition_tokens)
+                         partition_tokens=w.partition_tokens if partition_tokens is None else partition_tokens,
+                         flags=flags)
     cb = None if w.preset == "k8v4" else tq.tq_build_codebook(w.d, 3 if w.preset.startswith("k3") else 4)
     cache = torch.from_numpy(cache_np).cuda()
     lens = (inp.seq_lens if seq_lens is None else seq_lens).cuda()
@@ -91,6 +92,17 @@ def test_decode_partition_invariance(tq, pt):
     w, inp, oc, q, ref = oracle_case("gqa_small")
     got = gpu_decode(tq, w, inp, oc.cache, partition_tokens=pt)
     assert_decode_close(got, ref, torch.float32)
+
+
+# TQ_FLAG_INDICES_READY only moves the reads of lengths and block ids before
+# the split kernel's dependency wait: the same arithmetic, bit-identical output.
+@pytest.mark.parametrize("name", ["gqa_small", "k3v4_small", "long_small"])
+def test_decode_indices_ready_flag(tq, name):
+    w, inp, oc, q, ref = oracle_case(name)
+    plain = gpu_decode(tq, w, inp, oc.cache, partition_tokens=0)
+    early = gpu_decode(tq, w, inp, oc.cache, partition_tokens=0, flags=tq.TQ_FLAG_INDICES_READY)
+    assert np.array_equal(plain, early)
+    assert_decode_close(early, ref, torch.float32)
 
 
 # The reduce has two launch shapes: a CTA per query head when there are few

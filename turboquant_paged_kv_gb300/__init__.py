@@ -42,10 +42,13 @@ def lib_path() -> str:
     return _abi.lib_path()
 
 
+TQ_FLAG_INDICES_READY = 1   # include/tq.h: seq_lens / block_table not written by the previous kernel
+
+
 def make_config(preset: str | int, num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
-                block_size: int = 16, partition_tokens: int = 0) -> tq_config:
+                block_size: int = 16, partition_tokens: int = 0, flags: int = 0) -> tq_config:
     pid = PRESET_IDS[preset] if isinstance(preset, str) else int(preset)
-    return tq_config(pid, head_dim, block_size, num_q_heads, num_kv_heads, partition_tokens)
+    return tq_config(pid, head_dim, block_size, num_q_heads, num_kv_heads, partition_tokens, flags)
 
 
 def tq_build_codebook(head_dim: int, bits: int) -> tq_codebook:

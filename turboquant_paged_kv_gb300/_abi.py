@@ -45,7 +45,7 @@ TQ_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 class tq_config(ctypes.Structure):
     _fields_ = [("preset", ctypes.c_int), ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
                 ("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int),
-                ("partition_tokens", ctypes.c_int)]
+                ("partition_tokens", ctypes.c_int), ("flags", ctypes.c_int)]
 
 
 class tq_layout(ctypes.Structure):

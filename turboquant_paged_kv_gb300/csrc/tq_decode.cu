@@ -145,6 +145,7 @@ struct DecodeArgs {
   int qbuf_bytes;      // G * d * 2
   int dyn_bytes;
   float qscale;        // softmax scale * log2(e)
+  int early_indices;   // TQ_FLAG_INDICES_READY: lengths and block ids read before the dependency wait
   float cent[16];
 };
 
@@ -413,6 +414,15 @@ __device__ __forceinline__ void cursor_next(Cursor& u, const DecodeArgs& a) {
 // current one is issued, so their latency overlaps the wait for a free stage.
 __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_t qslots, uint32_t first,
                               uint32_t lut, uint32_t klut) {
+  // Everything that may read what the previous kernel wrote comes after
+  // grid_dep_wait(); with early_indices the lengths and block ids are not
+  // among it, so the range, its location and the first plan come before.
+  auto wait_previous = [&]() {
+    grid_dep_wait();
+    grid_dep_launch();
+    asm volatile("bar.arrive 1, %0;\n" ::"r"(blockDim.x) : "memory");
+  };
+  if (!a.early_indices) wait_previous();
   const int lane = threadIdx.x & 31;
   const bool mine = lane < W;
   const long long nw = static_cast<long long>(gridDim.x) * W;
@@ -445,7 +455,7 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
     for (int o_ = 1; o_ < 32; o_ <<= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o_);
     total += nt;
   }
-  if (blockIdx.x == 0 && __any_sync(0xffffffffu, too_long) && lane == 0) flag(a.status, TQ_DEV_SEQ_TOO_LONG);
+  const bool flag_too_long = blockIdx.x == 0 && __any_sync(0xffffffffu, too_long) && lane == 0;
   total *= a.n_kv;
   // range [total * wid / nw, total * (wid + 1) / nw), 32-bit division when it fits
   const bool narrow = total * nw < (1ll << 32);
@@ -524,6 +534,8 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
     for (int i = 0; i < n && rem > 0; ++i) cursor_next(pc, a);
   };
   if (mine && rem > 0) plan();
+  if (a.early_indices) wait_previous();
+  if (flag_too_long) flag(a.status, TQ_DEV_SEQ_TOO_LONG);
 
   const uint64_t policy = evict_first_policy();
   const long long blk_bytes = static_cast<long long>(a.n_kv) * a.tiles_per_block * a.tile_bytes;   // one cache block
@@ -739,17 +751,18 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
     l0 = l1 = z0 = z1 = 0.f;
   };
 
-  // the kChunk tiles of a stage at shared address st, in lock-step phases so
+  // NT (1 or 2) tiles of a stage at shared address st, in lock-step phases so
   // their accumulation chains interleave; tile i has nv[i] real positions
   // (tiles past the chunk's end compute on stale bytes and are fully masked)
-  auto chunk = [&](uint32_t st, const int (&nv)[kChunk]) {
+  auto chunk = [&](auto nt_tag, uint32_t st, const int* nv) {
+    constexpr int NT = decltype(nt_tag)::value;
     // ---- S_i = K_i . Q^T
-    float v[kChunk][4];   // [0] tok g col 2c, [1] tok g col 2c+1, [2] tok g+8 col 2c, [3] tok g+8 col 2c+1
+    float v[NT][4];   // [0] tok g col 2c, [1] tok g col 2c+1, [2] tok g+8 col 2c, [3] tok g+8 col 2c+1
     if constexpr (KMODE == kFp8) {
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
+      for (int i = 0; i < NT; ++i) v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
+      for (int i = 0; i < NT; ++i) {
         const uint32_t kt = st + i * a.tile_bytes + a.k_off;
         const uint4 kg0 = lds128(kt + g * 128 + 32 * c), kg1 = lds128(kt + g * 128 + 32 * c + 16);
         const uint4 kh0 = lds128(kt + (g + 8) * 128 + 32 * c), kh1 = lds128(kt + (g + 8) * 128 + 32 * c + 16);
@@ -769,9 +782,9 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
         }
       }
     } else {
-      uint4 kg[kChunk], kh[kChunk];   // this lane's key slices of tokens g and g+8
+      uint4 kg[NT], kh[NT];   // this lane's key slices of tokens g and g+8
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
+      for (int i = 0; i < NT; ++i) {
         const uint32_t kt = st + i * a.tile_bytes + a.k_off;
         if constexpr (KMODE == kMse4) {
           kg[i] = lds128(kt + g * 64 + 16 * c);
@@ -786,15 +799,15 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
       // 32c + 4s .. +3 (two key bytes = two LUT entries of two centroids each).
       // Two accumulators per tile (even and odd k-steps; G > 4: hi and lo query
       // parts) halve the dependent mma chains.
-      float va[kChunk][4], vb[kChunk][4];
+      float va[NT][4], vb[NT][4];
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i)
+      for (int i = 0; i < NT; ++i)
 #pragma unroll
         for (int k = 0; k < 4; ++k) va[i][k] = vb[i][k] = 0.f;
 #pragma unroll
       for (int s2 = 0; s2 < 8; ++s2) {
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
+        for (int i = 0; i < NT; ++i) {
           const uint32_t g0 = lds32(lut_addr<KMODE>(kg[i], 2 * s2, lut_lane));
           const uint32_t g1 = lds32(lut_addr<KMODE>(kg[i], 2 * s2 + 1, lut_lane));
           const uint32_t h0 = lds32(lut_addr<KMODE>(kh[i], 2 * s2, lut_lane));
@@ -810,7 +823,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
         }
       }
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i)
+      for (int i = 0; i < NT; ++i)
 #pragma unroll
         for (int k = 0; k < 4; ++k) v[i][k] = va[i][k] + vb[i][k];
     }
@@ -822,10 +835,10 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
       // g + 8 (its l, z are summed over the pair at the end), and one more
       // exchange gives each lane the other half of the P^T operands.
       const int tk = lo_lane ? g + 8 : g;
-      float t0[kChunk], t1[kChunk], sv[kChunk], sz[kChunk];
+      float t0[NT], t1[NT], sv[NT], sz[NT];
       float cm0 = -INFINITY, cm1 = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
+      for (int i = 0; i < NT; ++i) {
         const uint32_t tb = st + i * a.tile_bytes;
 #pragma unroll
         for (int k = 0; k < 4; ++k) v[i][k] += __shfl_xor_sync(0xffffffffu, v[i][k], 2);
@@ -864,7 +877,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
         }
       }
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
+      for (int i = 0; i < NT; ++i) {
         const float p0 = ex2(t0[i] - m0), p1 = ex2(t1[i] - m1);
         l0 += p0;
         l1 += p1;
@@ -892,10 +905,10 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
     }
 
     // ---- G > 4: every lane carries both of its tokens
-    float svg[kChunk], svh[kChunk], szg[kChunk], szh[kChunk];
+    float svg[NT], svh[NT], szg[NT], szh[NT];
     float cm0 = -INFINITY, cm1 = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
+    for (int i = 0; i < NT; ++i) {
       const uint32_t tb = st + i * a.tile_bytes;
       if (!GBIG) {
 #pragma unroll
@@ -939,7 +952,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
 
     // ---- probabilities, P^T operands (movmatrix), O^T += V^T . P^T
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
+    for (int i = 0; i < NT; ++i) {
       const float p0 = ex2(v[i][0] - m0), p1 = ex2(v[i][1] - m1);
       const float p2 = ex2(v[i][2] - m0), p3 = ex2(v[i][3] - m1);
       l0 += p0 + p2;
@@ -998,7 +1011,13 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
 #pragma unroll
       for (int i = 0; i < kChunk; ++i)
         nv[i] = (i < n && ((okm >> i) & 1u)) ? min(kTileTokens, len - tok0 - 16 * i) : 0;
-      chunk(sa, nv);
+      // a stage's tiles two at a time in lock step, an odd last tile alone
+#pragma unroll
+      for (int t0 = 0; t0 < kChunk; t0 += 2) {
+        if (t0 > 0 && n <= t0) break;
+        if (t0 + 1 < kChunk) chunk(std::integral_constant<int, 2>{}, sa + t0 * a.tile_bytes, nv + t0);
+        else chunk(std::integral_constant<int, 1>{}, sa + t0 * a.tile_bytes, nv + t0);
+      }
     }
     __syncwarp();   // every lane has read the stage: the producer may refill it
     if (lane == 0) mbar_arrive(fb + 8);
@@ -1046,10 +1065,7 @@ split_kernel(const DecodeArgs a) {
     for (int i = lane; i < 2 * W * kStages + W; i += 32) mbar_init(bars + 8 * i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     __syncwarp();
-    grid_dep_wait();
-    grid_dep_launch();
-    asm volatile("bar.arrive 1, %0;\n" ::"r"(blockDim.x) : "memory");
-    producer_warp(a, W, bars, qslots, first, lut, kLut);
+    producer_warp(a, W, bars, qslots, first, lut, kLut);   // waits for the previous kernel itself
   } else {
     if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent, threadIdx.x - 32, blockDim.x - 32);
     asm volatile("bar.sync 1, %0;\n" ::"r"(blockDim.x) : "memory");
@@ -1588,6 +1604,7 @@ tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* 
   a.dyn_bytes = 0;
   const float sm_scale = scale > 0.f ? scale : 0.088388347648318440f;   // 1/sqrt(128)
   a.qscale = sm_scale * 1.4426950408889634f;                              // log2(e)
+  a.early_indices = (cfg->flags & TQ_FLAG_INDICES_READY) ? 1 : 0;
   const float gamma = P.L.key_fp8 ? 1.f : centroid_scale(cb->centroids, cb->num_levels);
   a.qscale /= gamma;
   for (int i = 0; i < 16; ++i)

@@ -27,6 +27,7 @@ tq_status make_layout(const tq_config* cfg, tq_layout* out) {
   if (!preset_info(cfg->preset, &pi)) return TQ_ERR_INVALID_ARG;
   const int d = cfg->head_dim;
   if (d <= 0 || cfg->block_size <= 0 || cfg->num_kv_heads <= 0) return TQ_ERR_INVALID_ARG;
+  if (cfg->flags & ~TQ_FLAG_INDICES_READY) return TQ_ERR_INVALID_ARG;
   if (d != 128) return TQ_ERR_UNSUPPORTED;
   const int bs = cfg->block_size;
   if (bs != 16 && bs != 32 && bs != 64 && bs != 128) return TQ_ERR_UNSUPPORTED;

@@ -115,6 +115,20 @@ def test_decode_many_pairs(tq, pt):
     assert_decode_close(got, ref, torch.float32)
 
 
+# Many pairs and no fixed partitions, with empty and 1-token sequences: the
+# per-pair reduce shape writes the zero rows and merges one-record segments.
+def test_decode_many_pairs_empty_and_single_token(tq):
+    w, inp, oc, q, _ = oracle_case("k3v4_small", batch=40)
+    lens = inp.seq_lens.clone()
+    lens[0] = 0
+    lens[7] = 1
+    lens[39] = 0
+    ref = oc.decode(q, seq_lens=lens.numpy())
+    got = gpu_decode(tq, w, inp, oc.cache, seq_lens=lens, max_seq_len=int(inp.seq_lens.max()), partition_tokens=0)
+    assert np.all(got[0] == 0.0) and np.all(got[39] == 0.0)
+    assert_decode_close(got, ref, torch.float32)
+
+
 @pytest.mark.parametrize("bs", [32, 64, 128])
 def test_decode_block_sizes(tq, bs):
     w, inp, oc, q, ref = oracle_case("gqa_small", block_size=bs)

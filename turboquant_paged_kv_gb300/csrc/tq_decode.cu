@@ -754,7 +754,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
   // NT (1 or 2) tiles of a stage at shared address st, in lock-step phases so
   // their accumulation chains interleave; tile i has nv[i] real positions
   // (tiles past the chunk's end compute on stale bytes and are fully masked)
-  auto chunk = [&](auto nt_tag, uint32_t st, const int* nv) {
+  auto chunk = [&](auto nt_tag, uint32_t st, const int* nv, uint32_t release_bar) {
     constexpr int NT = decltype(nt_tag)::value;
     // ---- S_i = K_i . Q^T
     float v[NT][4];   // [0] tok g col 2c, [1] tok g col 2c+1, [2] tok g+8 col 2c, [3] tok g+8 col 2c+1
@@ -828,6 +828,22 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
         for (int k = 0; k < 4; ++k) v[i][k] = va[i][k] + vb[i][k];
     }
 
+    // ---- value words of the tiles, read now so the stage can be released
+    // before the softmax and O^T: the producer refills it half a chunk earlier
+    uint4 vwa[NT], vwb[NT];   // tokens 2c, 2c+1 and 2c+8, 2c+9 of this lane's 16-byte groups
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      const uint32_t vt = st + i * a.tile_bytes + a.v_off + 16 * (g ^ (2 * c));
+      vwa[i] = lds128(vt + 128 * c);
+      vwb[i] = lds128(vt + 128 * (c + 4));
+    }
+    auto release = [&]() {   // every lane has read the stage (values, norms, scales, zeros)
+      if (release_bar) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(release_bar);
+      }
+    };
+
     // ---- scores, probabilities and O^T += V^T . P^T
     if constexpr (!GBIG) {
       // G <= 4: after the hi/lo exchange lanes c and c ^ 2 hold the same
@@ -860,6 +876,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
         cm0 = fmaxf(cm0, x0);
         cm1 = fmaxf(cm1, x1);
       }
+      release();
       if (__any_sync(0xffffffffu, cm0 > m0 + kTau || cm1 > m1 + kTau)) {   // rare: move the max, rescale
 #pragma unroll
         for (int o_ = 2; o_ < 32; o_ <<= 1) {
@@ -889,9 +906,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
         // b1 (tokens 8..15) the same: each lane lacks one of the two
         const uint32_t recv = __shfl_xor_sync(0xffffffffu, lo_lane ? hi : lo, 2);
         const uint32_t b0 = movmatrix_trans(lo_lane ? recv : hi), b1 = movmatrix_trans(lo_lane ? lo : recv);
-        const uint32_t vt = st + i * a.tile_bytes + a.v_off + 16 * (g ^ (2 * c));
-        const uint4 va = lds128(vt + 128 * c);         // tokens 2c, 2c+1
-        const uint4 vb = lds128(vt + 128 * (c + 4));   // tokens 2c+8, 2c+9
+        const uint4 va = vwa[i], vb = vwb[i];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t wa = word_of(va, k), wb = word_of(vb, k);
@@ -933,6 +948,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
       cm0 = fmaxf(cm0, fmaxf(v[i][0], v[i][2]));
       cm1 = fmaxf(cm1, fmaxf(v[i][1], v[i][3]));
     }
+    release();
     if (__any_sync(0xffffffffu, cm0 > m0 + kTau || cm1 > m1 + kTau)) {   // rare: move the max, rescale
 #pragma unroll
       for (int o_ = 4; o_ < 32; o_ <<= 1) {
@@ -965,9 +981,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
       const uint32_t b0 = movmatrix_trans(lo_lane ? lg : hg), b1 = movmatrix_trans(lo_lane ? lh : hh);
       uint32_t b0l = 0u, b1l = 0u;
       if (GBIG) { b0l = movmatrix_trans(lg); b1l = movmatrix_trans(lh); }
-      const uint32_t vt = st + i * a.tile_bytes + a.v_off + 16 * (g ^ (2 * c));
-      const uint4 va = lds128(vt + 128 * c);         // tokens 2c, 2c+1
-      const uint4 vb = lds128(vt + 128 * (c + 4));   // tokens 2c+8, 2c+9
+      const uint4 va = vwa[i], vb = vwb[i];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t wa = word_of(va, k), wb = word_of(vb, k);
@@ -1011,16 +1025,19 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
 #pragma unroll
       for (int i = 0; i < kChunk; ++i)
         nv[i] = (i < n && ((okm >> i) & 1u)) ? min(kTileTokens, len - tok0 - 16 * i) : 0;
-      // a stage's tiles two at a time in lock step, an odd last tile alone
+      // a stage's tiles two at a time in lock step, an odd last tile alone; the
+      // last call releases the stage once it has read it
 #pragma unroll
       for (int t0 = 0; t0 < kChunk; t0 += 2) {
         if (t0 > 0 && n <= t0) break;
-        if (t0 + 1 < kChunk) chunk(std::integral_constant<int, 2>{}, sa + t0 * a.tile_bytes, nv + t0);
-        else chunk(std::integral_constant<int, 1>{}, sa + t0 * a.tile_bytes, nv + t0);
+        const uint32_t rel = t0 + 2 >= kChunk || n <= t0 + 2 ? fb + 8 : 0u;
+        if (t0 + 1 < kChunk) chunk(std::integral_constant<int, 2>{}, sa + t0 * a.tile_bytes, nv + t0, rel);
+        else chunk(std::integral_constant<int, 1>{}, sa + t0 * a.tile_bytes, nv + t0, rel);
       }
+    } else {
+      __syncwarp();   // every lane has read the descriptor: the producer may refill the stage
+      if (lane == 0) mbar_arrive(fb + 8);
     }
-    __syncwarp();   // every lane has read the stage: the producer may refill it
-    if (lane == 0) mbar_arrive(fb + 8);
     cs = cs + 1 == kStages ? 0 : cs + 1;
     if (last) break;
   }

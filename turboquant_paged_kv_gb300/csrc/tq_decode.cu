@@ -33,7 +33,9 @@
 //  stage's "full" mbarrier. A chunk that opens a segment also brings the
 //  segment's query rows into the consumer's query slot, once the consumer has
 //  taken the previous rows ("q empty" mbarrier). Consumers only read
-//  descriptors and compute, and release a stage through its "empty" mbarrier.
+//  descriptors and compute, and release a stage through its "empty" mbarrier
+//  as soon as they have read it (after QK and the score loads, with the value
+//  words in registers), half a chunk before they are done with its math.
 //  The producer starts as soon as the barriers exist; the consumers build the
 //  LUT meanwhile. Every wait is bounded: a consumer whose wait expires flags
 //  TQ_DEV_TIMEOUT and stops; the producer gives up after a long stretch
@@ -102,6 +104,9 @@ constexpr int kMaxConsumers = TQ_DECODE_WARPS;   // consumer warps per CTA (fewe
 #endif
 #ifndef TQ_PRODUCER_SLEEP_NS
 #define TQ_PRODUCER_SLEEP_NS 64
+#endif
+#ifndef TQ_PRODUCER_PASSES
+#define TQ_PRODUCER_PASSES 1   // chunks a producer lane may issue per pass
 #endif
 constexpr int kChunk = TQ_DECODE_CHUNK;     // tiles per ring stage
 constexpr int kStages = TQ_DECODE_STAGES;   // ring stages per consumer warp
@@ -552,9 +557,6 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
   int idle = 0;
   while (__any_sync(0xffffffffu, !done)) {
     bool progressed = false;
-#ifndef TQ_PRODUCER_PASSES
-#define TQ_PRODUCER_PASSES 1
-#endif
     // one chunk per lane per pass: the block ids plan() loads for the next
     // chunk are only read on the next pass, after other lanes' work
     for (int pass = 0; pass < TQ_PRODUCER_PASSES && !done; ++pass) {

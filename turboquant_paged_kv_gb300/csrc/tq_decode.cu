@@ -295,6 +295,17 @@ __device__ __forceinline__ void fwht128(float v[4], int lane) {
   }
 }
 
+// *p if pred, else dflt: a predicated load into a preset register, so nothing
+// consumes the loaded value here and the warp does not wait for it (a select
+// on the loaded value would); the address is not touched when !pred.
+__device__ __forceinline__ int ldg_or(const int* p, bool pred, int dflt) {
+  int v = dflt;
+  asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q ld.global.nc.b32 %0, [%1];\n}\n"
+               : "+r"(v)
+               : "l"(p), "r"(static_cast<unsigned>(pred)));
+  return v;
+}
+
 __device__ __forceinline__ void flag(unsigned int* status, unsigned int bit) {
   if (status) atomicOr(status, bit);
 }
@@ -534,7 +545,7 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
     n_seg = (pc.b * a.n_kv + pc.h) * a.num_parts + (a.part_tiles > 0 ? pc.t / a.part_tiles : 0);
     const int* row = a.block_table + static_cast<long long>(pc.b) * a.bt_stride;
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) n_blk[i] = i < n ? __ldg(row + (((pc.t + i) << 4) >> a.log2_bs)) : -1;
+    for (int i = 0; i < kChunk; ++i) n_blk[i] = ldg_or(row + (((pc.t + i) << 4) >> a.log2_bs), i < n, -1);
     rem -= n;
     for (int i = 0; i < n && rem > 0; ++i) cursor_next(pc, a);
   };

@@ -28,5 +28,7 @@ Modules:
   numerics  fp16 / e4m3 encodings and the fp32 value-quantisation steps.
   layout    preset table, slot sizes and the paged tile layout (byte addresses).
   store     quantise K/V vectors and write slots into a paged cache.
-  decode    attention over the packed cache (exact softmax, no split).
+  decode    attention over the packed cache (exact softmax, no split), and the
+            continuation-chunk form of it (one decode request per query).
+  dequant   the cached keys and values expanded back to the original basis.
 """

@@ -31,7 +31,7 @@ from . import numerics, rotation
 from .layout import Preset, TileLayout, TILE_TOKENS, v_word_offset
 from .store import unpack_bits
 
-__all__ = ["read_positions", "dequantized_values", "decode"]
+__all__ = ["read_positions", "dequantized_values", "decode", "continuation_decode"]
 
 _E4M3 = numerics.e4m3_decode_table()
 
@@ -117,3 +117,21 @@ def decode(q: np.ndarray, cache: np.ndarray, layout: TileLayout, preset: Preset,
                 p = np.exp(scores - scores.max())
                 out[b, h] = (p @ vhat) / p.sum()
     return out
+
+
+def continuation_decode(q_chunk: np.ndarray, cache: np.ndarray, layout: TileLayout, preset: Preset,
+                        centroids, block_row: np.ndarray, cached_len: int,
+                        scale: float | None = None) -> np.ndarray:
+    """Attention of the q_len queries of a continuation chunk, float64 [q_len, n_q, d].
+
+    Restates [vLLM-TQ] section "续写 prefill:小 chunk 走 decode,大 chunk 走反量化":
+    the chunk's keys and values are already in the cache, and query i of the
+    chunk (0-based) is served as a decode request of length cached_len + i + 1
+    over the sequence's one block-table row, which is what makes the attention
+    causal without a mask.
+    """
+    q_chunk = np.asarray(q_chunk, dtype=np.float64)
+    q_len = q_chunk.shape[0]
+    table = np.broadcast_to(np.asarray(block_row)[None, :], (q_len, len(block_row)))
+    lens = cached_len + 1 + np.arange(q_len)
+    return decode(q_chunk, cache, layout, preset, centroids, table, lens, scale)

@@ -15,6 +15,7 @@ L2 hygiene: three copies of the cache (3 x 143 MB, each larger than L2) are
 rotated between steps, so no step finds its cache in L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
+  python bench.py --op dequant [--steps K] [--warmup W]   (full dequantisation alone)
 
 ``--impl reference`` times the CPU oracle (test infrastructure) on a bounded
 sample of the same workload; N > 1 runs weak-scaling replicas (each rank its
@@ -394,6 +395,74 @@ def run_tq(args):
     return 0
 
 
+def run_dequant(args):
+    """``--op dequant``: tq_dequant of the whole gqa cache (32 x 4096 positions,
+    8 KV heads) to bf16 keys and values in the original basis, one launch per
+    step, timed alone with CUDA events. Each launch reads 141 MB of packed
+    slots and writes 537 MB, far more than L2, so consecutive launches find
+    nothing in L2.
+    Prints one JSON line of its own (not the decode step's)."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from turboquant_paged_kv_gb300 import build as tqbuild
+    tqbuild.build()
+    import turboquant_paged_kv_gb300 as tq
+    import workloads
+
+    w = workloads.get(WORKLOAD)
+    inp = workloads.make_inputs(w, device=dev)
+    cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size)
+    cb = tq.tq_build_codebook(w.d, 4)
+    lay = tq.tq_layout_for(cfg)
+    cache = torch.empty(inp.num_blocks * lay.block_bytes, dtype=torch.uint8, device=dev)
+    for b in range(w.batch):
+        k, v = inp.kv_for_sequence(b, dev)
+        s0 = dict(inp.fill_order)[b]
+        tq.tq_store(cfg, cb, k, v, inp.fill_slots[s0: s0 + k.shape[0]], cache)
+    max_len = inp.max_seq_len
+    shape = (w.batch, max_len, w.n_kv, w.d)
+    k_out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    v_out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    positions = int(inp.seq_lens.sum().item()) * w.n_kv
+    nbytes = positions * (lay.slot_bytes + 2 * w.d * 2)    # packed slot in, bf16 key + value out
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tq.tq_dequant(cfg, cb, cache, inp.block_table, inp.seq_lens, max_len, k_out, v_out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else "0"
+    with ClockSampler(gpu_id) as clk:
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    peak, peak_src = _peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "op": "dequant", "metric": "full dequant GB/s (packed slots read + bf16 K/V written)",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "f32 arithmetic, bf16 out", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: {w.note}, d {w.d}, block {w.block_size}, {w.preset}, bf16 out",
+                   "l2": "each launch moves %.0f MB (> L2)" % (nbytes / 1e6), "bytes_per_launch": nbytes},
+        "roofline": {"kernel": "dequant_kernel (tq_dequant)", "bound": "hbm", "achieved": gbs, "peak": peak,
+                     "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src, "ms_per_launch": ms,
+                     "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,9 +471,13 @@ def main():
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="decode", choices=["decode", "dequant"],
+                    help="decode: the decode step (default); dequant: tq_dequant of the gqa cache alone")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.op == "dequant":
+        return run_dequant(args)
     return run_reference(args) if args.impl == "reference" else run_tq(args)
 
 

@@ -8,7 +8,7 @@
  *   [TQ-intro] "vLLM TurboQuant 介绍:极低比特 KV Cache 量化" (beaiera.top)
  *   [NVFP4-TQ] "NVIDIA KV Cache 量化中的 NVFP4 与 TurboQuant" (moonnryan.github.io)
  *
- * Two hot operations:
+ * Two hot operations, and one for long cached histories:
  *   tq_store   per (token, KV head): L2 norm, normalised Walsh-Hadamard
  *              rotation, Lloyd-Max bucketize, norm-correction fold, bit-pack
  *              of the K indices (or an e4m3 cast for FP8 keys), asymmetric
@@ -18,6 +18,8 @@
  *              the packed cache: split-K over partitions of the sequence with
  *              an online softmax, then an LSE-weighted reduce. No 16-bit copy
  *              of the cache is ever materialised.
+ *   tq_dequant the cached keys and values expanded back to dense vectors in
+ *              the original basis (continuation prefill over a long history).
  *
  * Conventions shared by every entry point
  *   - Ownership: the caller owns every buffer. The library allocates nothing,
@@ -256,6 +258,37 @@ tq_status tq_decode_noalloc(const tq_config* cfg, const tq_codebook* cb,
                             const int* seq_lens, int batch, int max_seq_len, float scale,
                             void* out, int out_dtype,
                             unsigned int* dev_status, tq_stream_t stream);
+
+/* Device. The cached keys and values of `batch` sequences expanded back to
+ * dense vectors in the original (unrotated) basis, for callers that run
+ * attention outside this library over a long cached history (the pages'
+ * continuation-prefill path: [vLLM-TQ] section "续写 prefill:小 chunk 走 decode,
+ * 大 chunk 走反量化", subsection "反量化 kernel:_tq_full_dequant_kv"):
+ *   index-coded keys  k = stored_norm * (H / sqrt(d)) c[idx]  (the rotation is
+ *                     its own inverse)
+ *   FP8 keys          k = e4m3 value
+ *   values            v = fp16(scale) * code + fp16(zero)
+ * computed in fp32 and rounded once to out_dtype.
+ *   cfg, cb       host; as for tq_decode (cb ignored for TQ_PRESET_K8V4;
+ *                 num_q_heads is not used)
+ *   cache, num_blocks, block_table, bt_stride, seq_lens, batch, max_seq_len
+ *                 device / sizes, exactly as for tq_decode
+ *   key_out, value_out  device [batch][max_seq_len][n_kv][d] of out_dtype
+ *                 (f16, bf16 or f32), 16-byte aligned, owned by the caller;
+ *                 every element is written: positions at or past
+ *                 min(seq_lens[b], max_seq_len, bt_stride * block_size) are 0
+ *   dev_status    device uint32 or NULL: TQ_DEV_SEQ_TOO_LONG for a length
+ *                 above that cap (the sequence is cut there),
+ *                 TQ_DEV_BLOCK_OUT_OF_RANGE for a block id outside
+ *                 [0, num_blocks) (its positions are written as 0)
+ * batch == 0 or max_seq_len == 0 is a no-op. One launch, one warp per
+ * (sequence, position, KV head); no workspace. */
+tq_status tq_dequant(const tq_config* cfg, const tq_codebook* cb,
+                     const void* cache, long long num_blocks,
+                     const int* block_table, int bt_stride,
+                     const int* seq_lens, int batch, int max_seq_len,
+                     void* key_out, void* value_out, int out_dtype,
+                     unsigned int* dev_status, tq_stream_t stream);
 
 /* Host. Static description of a status code. */
 const char* tq_status_string(int status);

@@ -125,3 +125,39 @@ def test_host_argument_errors_return_before_launch(tq):
     assert dec(uneven, 1 << 30) == _abi.TQ_ERR_INVALID_ARG
     badpart = tq.make_config("4bit_nc", 32, 8, partition_tokens=40)
     assert dec(badpart, 1 << 30) == _abi.TQ_ERR_INVALID_ARG
+
+
+def test_dequant_argument_errors_return_before_launch(tq):
+    from turboquant_paged_kv_gb300 import _abi
+    lib = _abi.load()
+    cfg = tq.make_config("4bit_nc", 32, 8)
+    cb = tq.tq_build_codebook(128, 4)
+    cb3 = tq.tq_build_codebook(128, 3)
+    ok16 = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    odd4 = ctypes.c_void_p(0x10002)
+
+    def dq(cfg_=cfg, cb_=cb, cache=ok16, table=ok16, stride=4, lens=ok16, batch=2, max_len=64,
+           kout=ok16, vout=ok16, dtype=1, status=None):
+        return lib.tq_dequant(ctypes.byref(cfg_), None if cb_ is None else ctypes.byref(cb_), cache, 10, table,
+                              stride, lens, batch, max_len, kout, vout, dtype, status, None)
+
+    # empty requests are no-ops even with null pointers
+    assert dq(cache=None, table=None, lens=None, kout=None, vout=None, batch=0) == _abi.TQ_OK
+    assert dq(cache=None, table=None, lens=None, kout=None, vout=None, max_len=0) == _abi.TQ_OK
+    assert dq(kout=None) == _abi.TQ_ERR_INVALID_ARG
+    assert dq(lens=None) == _abi.TQ_ERR_INVALID_ARG
+    assert dq(vout=odd) == _abi.TQ_ERR_MISALIGNED
+    assert dq(cache=odd) == _abi.TQ_ERR_MISALIGNED
+    assert dq(table=odd4) == _abi.TQ_ERR_MISALIGNED
+    assert dq(status=odd4) == _abi.TQ_ERR_MISALIGNED
+    assert dq(cb_=cb3) == _abi.TQ_ERR_INVALID_ARG        # codebook of the wrong width
+    assert dq(cb_=None) == _abi.TQ_ERR_INVALID_ARG
+    assert dq(dtype=7) == _abi.TQ_ERR_INVALID_ARG
+    assert dq(stride=0) == _abi.TQ_ERR_INVALID_ARG
+    assert dq(batch=-1) == _abi.TQ_ERR_INVALID_ARG
+    assert dq(cfg_=tq.make_config("3bit_nc", 32, 8), cb_=cb3) == _abi.TQ_ERR_UNSUPPORTED
+    assert dq(cfg_=tq.make_config("4bit_nc", 32, 8, block_size=24)) == _abi.TQ_ERR_UNSUPPORTED
+    # FP8 keys need no codebook; this call would launch, so only the argument
+    # checks that come first are exercised
+    assert dq(cfg_=tq.make_config("k8v4", 32, 8), cb_=None, kout=None) == _abi.TQ_ERR_INVALID_ARG

@@ -34,6 +34,7 @@ _DTYPES = {torch.float16: TQ_DTYPE_F16, torch.bfloat16: TQ_DTYPE_BF16, torch.flo
 
 __all__ = ["make_config", "tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode",
            "tq_decode_partials", "tq_decode_reduce", "tq_decode_noalloc", "tq_decode_workspace_size",
+           "tq_dequant",
            "tq_status_string",
            "tq_version", "TQError", "lib_path"]
 
@@ -150,3 +151,18 @@ def tq_decode_reduce(cfg: tq_config, seq_lens: torch.Tensor, batch: int, max_seq
     _abi.check("tq_decode_reduce", _LIB.tq_decode_reduce(
         ctypes.byref(cfg), _ptr(seq_lens), batch, max_seq_len, bt_stride, _ptr(out), _DTYPES[out.dtype],
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def tq_dequant(cfg: tq_config, cb, cache: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+               max_seq_len: int, key_out: torch.Tensor, value_out: torch.Tensor, num_blocks: int | None = None,
+               dev_status: torch.Tensor | None = None, stream=None) -> None:
+    """key_out, value_out [B, max_seq_len, n_kv, d] (f16, bf16 or f32), written in full."""
+    if value_out.dtype != key_out.dtype:
+        raise ValueError("key_out and value_out must have the same dtype")
+    lay = tq_layout_for(cfg)
+    if num_blocks is None:
+        num_blocks = cache.numel() // lay.block_bytes
+    _abi.check("tq_dequant", _LIB.tq_dequant(
+        ctypes.byref(cfg), _cb(cb), _ptr(cache), num_blocks, _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), seq_lens.shape[0], max_seq_len, _ptr(key_out), _ptr(value_out),
+        _DTYPES[key_out.dtype], _ptr(dev_status), _stream(stream)))

@@ -37,7 +37,7 @@ TQ_DEV_TIMEOUT = 8
 # every function tq.h declares (checked by the ABI tests)
 EXPORTED = ("tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode_workspace_size",
             "tq_decode", "tq_decode_partials", "tq_decode_reduce", "tq_decode_noalloc",
-            "tq_status_string", "tq_version")
+            "tq_dequant", "tq_status_string", "tq_version")
 
 TQ_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -83,6 +83,8 @@ _SIGS = {
     "tq_decode_reduce": (_i, [ctypes.POINTER(tq_config), _vp, _i, _i, _i, _vp, _i, _vp, _sz, _vp]),
     "tq_decode_noalloc": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_codebook), _vp, _i, _vp, _ll,
                                _vp, _i, _vp, _i, _i, _f, _vp, _i, _vp, _vp]),
+    "tq_dequant": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_codebook), _vp, _ll, _vp, _i, _vp, _i,
+                        _i, _vp, _vp, _i, _vp, _vp]),
     "tq_status_string": (ctypes.c_char_p, [_i]),
     "tq_version": (_i, []),
 }

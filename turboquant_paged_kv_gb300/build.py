@@ -28,7 +28,7 @@ NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I" + INCLUDE, "-I" + CSRC]
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
-CU_SOURCES = ["tq_store.cu", "tq_decode.cu", "tq_decode_noalloc.cu"]
+CU_SOURCES = ["tq_store.cu", "tq_decode.cu", "tq_decode_noalloc.cu", "tq_dequant.cu"]
 CPP_SOURCES = ["tq_host.cpp"]
 
 

@@ -14,6 +14,11 @@ prefill chunk) and the split kernel's roofline.
 L2 hygiene: three copies of the cache (3 x 143 MB, each larger than L2) are
 rotated between steps, so no step finds its cache in L2.
 
+The K timed steps are launched eagerly through the binding. The same K steps
+replayed from CUDA graphs (one captured step per cache copy, as a serving loop
+replays its decode step) are timed too and reported as ``graph_ms_per_step``
+(null, with ``config.graph`` saying why, if capture fails).
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
   python bench.py --op dequant [--steps K] [--warmup W]   (full dequantisation alone)
 
@@ -285,7 +290,37 @@ def run_tq(args):
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        step_ms = ev0.elapsed_time(ev1) / args.steps
+        eager_ms = ev0.elapsed_time(ev1) / args.steps
+
+        # ---- the same K steps replayed from CUDA graphs (one per cache copy),
+        # as a serving loop runs its decode step
+        graph_ms, graph_note, graphs = None, "captured", []
+        try:
+            for c in range(n_copies):
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr):
+                    step(c)
+                graphs.append(gr)
+        except RuntimeError as exc:   # capture refused: only the eager steps count
+            graphs, graph_note = [], "capture failed: %s" % str(exc).splitlines()[0][:120]
+        # every rank times the graphs only if every rank captured them
+        if max_over_ranks([0.0 if graphs else 1.0], dev, world)[0] == 0.0:
+            for i in range(args.warmup):
+                graphs[i % n_copies].replay()
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            ev0.record(stream)
+            for i in range(args.steps):
+                graphs[i % n_copies].replay()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            graph_ms = ev0.elapsed_time(ev1) / args.steps
+        elif graphs:
+            graph_note = "capture failed on another rank"
+        step_ms = eager_ms
 
         # ---- split kernel alone (the dominant kernel), same stream, rotated caches
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -352,7 +387,10 @@ def run_tq(args):
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
     # ---- max over ranks
-    step_ms, split_ms, store_ms, e2e_ms = max_over_ranks([step_ms, split_ms, store_ms, e2e_ms], dev, world)
+    # one collective for every rank, whether or not its capture worked
+    step_ms, split_ms, store_ms, e2e_ms, graph_max, graph_failed = max_over_ranks(
+        [step_ms, split_ms, store_ms, e2e_ms, graph_ms or 0.0, 1.0 if graph_ms is None else 0.0], dev, world)
+    graph_ms = None if graph_failed else graph_max
     clocks = clk.summary()
 
     if rank == 0:
@@ -366,7 +404,8 @@ def run_tq(args):
             "config": {"workload": f"{WORKLOAD}: {w.note}, d {w.d}, block {w.block_size}, {w.preset}, bf16 in/out",
                        "partition_tokens": args.partition, "split": "stream-K: equal tile ranges per warp" if args.partition == 0 else "fixed partitions",
                        "l2": "3 rotated cache copies of %.0f MB each (> L2)" % (caches[0].numel() / 1e6),
-                       "kv_bytes_per_step": kv_bytes},
+                       "kv_bytes_per_step": kv_bytes, "graph": graph_note},
+            "graph_ms_per_step": graph_ms,
             "decode_tok_s": world * B / (step_ms * 1e-3),
             "hbm_frac_step": gbs / world / peak,
             "store_mtok_s": n_store / (store_ms * 1e-3) / 1e6,

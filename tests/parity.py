@@ -10,7 +10,16 @@ Tolerances (from the method's stated gates):
     oracle's norm for the GPU's own indices, so a boundary flip elsewhere in
     the vector does not count twice);
   * decode output: max |gpu - oracle| <= 2e-3 on fp32 output; for bf16/fp16
-    output 2e-3 plus half an output ulp of the oracle value.
+    output 2e-3 plus half an output ulp of the oracle value;
+  * full dequant (derived from its arithmetic): index-coded keys within
+    1e-6 * ||k|| per vector on fp32 output (stored_norm * c[idx] is one
+    rounding, the 7 butterfly stages one each and the 1 / sqrt(d) scale one,
+    so the error is at most 9 * 2^-24 * sum |stored_norm * c[idx_i]| / sqrt(d)
+    <= 9 * 2^-24 * ||k||); FP8 keys exact (every e4m3 value is an f16, bf16
+    and f32 value); values exactly the fp32 rounding of the oracle's value (one
+    fused multiply-add of fp16 scale, integer code and fp16 zero); 16-bit
+    outputs that plus half an output ulp (at least half the type's smallest
+    subnormal step).
 """
 
 from __future__ import annotations
@@ -164,3 +173,31 @@ def unquantized_attention(q: np.ndarray, kv, n_kv: int, scale=None):
             e = np.exp(s - s.max())
             out[b, h] = (e / e.sum()) @ v[:, h // group]
     return out
+
+
+_MANT = {torch.bfloat16: 8, torch.float16: 11, torch.float32: 24}
+_MIN_HALF_STEP = {torch.bfloat16: 2.0 ** -134, torch.float16: 2.0 ** -25, torch.float32: 2.0 ** -150}
+
+
+def _half_ulp_floor(x, dtype):
+    ax = np.maximum(np.abs(x), 1e-300)
+    return np.maximum(0.5 * np.exp2(np.floor(np.log2(ax)) - (_MANT[dtype] - 1)), _MIN_HALF_STEP[dtype])
+
+
+def assert_dequant_close(gk, gv, rk, rv, dtype, fp8_keys):
+    """Element-by-element gate of the module docstring; returns the max errors."""
+    assert np.all(np.isfinite(gk)) and np.all(np.isfinite(gv)), "an output element was not written"
+    ek = np.abs(gk - rk)
+    if fp8_keys:
+        assert np.all(ek == 0), f"FP8 key mismatch {ek.max():.3e}"
+    else:
+        tol32 = 1e-6 * np.linalg.norm(rk, axis=-1, keepdims=True)
+        tol = tol32 if dtype == torch.float32 else tol32 + _half_ulp_floor(np.abs(rk) + tol32, dtype)
+        assert np.all(ek <= tol), f"key error {ek.max():.3e} over tolerance"
+    ev = np.abs(gv - rv)
+    if dtype == torch.float32:
+        assert np.array_equal(gv, rv.astype(np.float32).astype(np.float64)), f"value mismatch {ev.max():.3e}"
+    else:
+        tol = 2.0 ** -24 * np.abs(rv) + _half_ulp_floor(np.abs(rv) * (1 + 2.0 ** -23), dtype)
+        assert np.all(ev <= tol), f"value error {ev.max():.3e} over tolerance"
+    return float(ek.max()), float(ev.max())

@@ -209,3 +209,61 @@ def test_decode_all_sequences_empty(tq, pt):
     lens = torch.zeros_like(inp.seq_lens)
     got = gpu_decode(tq, w, inp, oc.cache, seq_lens=lens, max_seq_len=16, partition_tokens=pt)
     assert np.all(got == 0.0)
+
+
+@pytest.mark.parametrize("pt", [None, 0])
+def test_store_decode_dequant_capture_in_cuda_graph(tq, pt):
+    # the calls only enqueue kernels (no allocation, no synchronisation), so a
+    # serving step can be captured once and replayed: the replay must give
+    # the eager results bit for bit, and the oracle's within the gates
+    w, inp, oc, q, ref = oracle_case("gqa_small")
+    cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size,
+                         partition_tokens=w.partition_tokens if pt is None else pt)
+    cb = tq.tq_build_codebook(w.d, 4)
+    dev = torch.device("cuda", 0)
+    base = torch.from_numpy(oc.cache).to(dev)
+    cache = base.clone()
+    table = inp.block_table.to(dev)
+    lens = inp.seq_lens.to(dev)
+    msl = inp.max_seq_len
+    qd = inp.q.to(dev)
+    # one new token per sequence, written over its last cached position
+    g = torch.Generator().manual_seed(3)
+    new_k = torch.randn((w.batch, w.n_kv, w.d), generator=g).to(torch.bfloat16).to(dev)
+    new_v = torch.randn((w.batch, w.n_kv, w.d), generator=g).to(torch.bfloat16).to(dev)
+    last = inp.seq_lens.to(torch.int64) - 1
+    slots = (inp.block_table[torch.arange(w.batch), last // w.block_size].to(torch.int64) * w.block_size
+             + last % w.block_size).to(dev)
+    out = torch.empty((w.batch, w.n_q, w.d), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_decode_workspace_size(cfg, w.batch, msl), dtype=torch.uint8, device=dev)
+    kout = torch.empty((w.batch, msl, w.n_kv, w.d), dtype=torch.bfloat16, device=dev)
+    vout = torch.empty_like(kout)
+
+    def step():
+        tq.tq_store(cfg, cb, new_k, new_v, slots, cache)
+        tq.tq_decode(cfg, cb, qd, cache, table, lens, msl, out, ws)
+        tq.tq_dequant(cfg, cb, cache, table, lens, msl, kout, vout)
+
+    step()
+    torch.cuda.synchronize()
+    eager = (cache.clone(), out.clone(), kout.clone(), vout.clone())
+    cache.copy_(base)
+    out.zero_()
+    kout.zero_()
+    vout.zero_()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    cache.copy_(base)                  # capture ran nothing; start from the same cache
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, (cache, out, kout, vout)):
+        assert torch.equal(a, b)
+    # the oracle: the same new tokens stored by the oracle, then its decode
+    oc2 = OracleCache(w, inp).fill()
+    from oracle import store as ost
+    ost.store(new_k.double().cpu().numpy(), new_v.double().cpu().numpy(), slots.cpu().numpy(), oc2.cache, oc2.lay,
+              oc2.preset, oc2.cent, oc2.mid)
+    ref2 = oc2.decode(q)
+    assert_decode_close(out.cpu().numpy(), ref2, torch.float32)

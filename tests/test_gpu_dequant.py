@@ -4,17 +4,8 @@ oracle (through the C ABI binding).
 The GPU reads ORACLE-written caches, so both sides expand identical packed
 bytes and no oracle input comes from the CUDA path.
 
-Tolerances, derived from the arithmetic:
-  * keys (index-coded), fp32 output: the kernel forms stored_norm * c[idx]
-    (one rounding), runs the 7 butterfly stages (one rounding each) and scales
-    by fp32(1 / sqrt(d)) (one rounding), so each output is within
-    9 * 2^-24 * sum_i |stored_norm * c[idx_i]| / sqrt(d) <= 9 * 2^-24 * ||k||
-    of the exact value; the gate is 1e-6 * ||k|| per vector;
-  * FP8 keys: exact (every e4m3 value is an f16, bf16 and f32 value);
-  * values, fp32 output: a single fused multiply-add of fp16 scale, integer
-    code and fp16 zero, so exactly the fp32 rounding of the oracle's value;
-  * 16-bit outputs: the fp32 gate plus half an output ulp (at least half the
-    smallest subnormal step of the type).
+The gates are those of ``parity.assert_dequant_close`` (derived there from
+the kernel's arithmetic) and, for the continuation chunks, the decode gate.
 """
 
 import numpy as np
@@ -24,13 +15,9 @@ import torch
 import workloads
 from oracle import decode as od
 from oracle import dequant as dq
-from parity import OracleCache, assert_decode_close
+from parity import OracleCache, assert_decode_close, assert_dequant_close
 
 pytestmark = pytest.mark.gpu
-
-_MANT = {torch.bfloat16: 8, torch.float16: 11, torch.float32: 24}
-_MIN_HALF_STEP = {torch.bfloat16: 2.0 ** -134, torch.float16: 2.0 ** -25, torch.float32: 2.0 ** -150}
-
 
 @pytest.fixture(scope="module")
 def tq():
@@ -73,30 +60,6 @@ def gpu_dequant(tq, w, inp, cache_np, out_dtype=torch.float32, seq_lens=None, bl
                   dev_status=status)
     torch.cuda.synchronize()
     return kout.float().cpu().numpy(), vout.float().cpu().numpy()
-
-
-def _half_ulp(x, dtype):
-    ax = np.maximum(np.abs(x), 1e-300)
-    return np.maximum(0.5 * np.exp2(np.floor(np.log2(ax)) - (_MANT[dtype] - 1)), _MIN_HALF_STEP[dtype])
-
-
-def assert_dequant_close(gk, gv, rk, rv, dtype, fp8_keys):
-    """Element-by-element gate of the module docstring; returns the max errors."""
-    assert np.all(np.isfinite(gk)) and np.all(np.isfinite(gv)), "an output element was not written"
-    ek = np.abs(gk - rk)
-    if fp8_keys:
-        assert np.all(ek == 0), f"FP8 key mismatch {ek.max():.3e}"
-    else:
-        tol32 = 1e-6 * np.linalg.norm(rk, axis=-1, keepdims=True)
-        tol = tol32 if dtype == torch.float32 else tol32 + _half_ulp(np.abs(rk) + tol32, dtype)
-        assert np.all(ek <= tol), f"key error {ek.max():.3e} over tolerance"
-    ev = np.abs(gv - rv)
-    if dtype == torch.float32:
-        assert np.array_equal(gv, rv.astype(np.float32).astype(np.float64)), f"value mismatch {ev.max():.3e}"
-    else:
-        tol = 2.0 ** -24 * np.abs(rv) + _half_ulp(np.abs(rv) * (1 + 2.0 ** -23), dtype)
-        assert np.all(ev <= tol), f"value error {ev.max():.3e} over tolerance"
-    return float(ek.max()), float(ev.max())
 
 
 def oracle_dequant(oc, seq_lens, block_table, max_seq_len):

@@ -296,7 +296,7 @@ const char* tq_status_string(int status);
 /* Host. ABI version of this header (major * 100 + minor). */
 int tq_version(void);
 
-#define TQ_ABI_VERSION 100
+#define TQ_ABI_VERSION 101   /* 1.01: tq_dequant added */
 
 #ifdef __cplusplus
 }

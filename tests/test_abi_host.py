@@ -40,7 +40,9 @@ def test_every_declared_symbol_is_exported(tq):
     for name in declared:
         assert hasattr(lib, name), name
     assert sorted(_abi.EXPORTED) == declared
-    assert tq.tq_version() == 100
+    # matches the header's TQ_ABI_VERSION
+    text = open(os.path.join(ROOT, "include", "tq.h")).read()
+    assert tq.tq_version() == int(re.search(r"#define TQ_ABI_VERSION (\d+)", text).group(1)) == 101
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])

@@ -141,3 +141,14 @@ def test_gqa_head_mapping():
     got = od.decode(inp.q.double().numpy(), cache, lay, preset, c, inp.block_table.numpy(), inp.seq_lens.numpy())
     for h in range(32):
         np.testing.assert_allclose(got[:, h], 0.25 * (h // 4 + 1), atol=1e-12)
+
+
+@pytest.mark.parametrize("name", ["tiny", "gqa_small"])
+def test_decode_matches_brute_force_3bit_values(name):
+    # 3bit_nc: 3-bit keys and 3-bit values (48-byte value rows, no swizzle)
+    w, inp, preset, lay, c, cache, _, _ = build(name, preset="3bit_nc")
+    assert preset.value_bits == 3 and lay.vb == 48
+    q = inp.q.double().numpy()
+    got = od.decode(q, cache, lay, preset, c, inp.block_table.numpy(), inp.seq_lens.numpy())
+    ref = brute_force(w, inp, preset, lay, c, cache, q)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-10)

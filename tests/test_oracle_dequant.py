@@ -38,9 +38,10 @@ def _dequant(name, **over):
     return w, inp, preset, lay, c, cache, ks, vs, kh, vh
 
 
-@pytest.mark.parametrize("name", ["tiny", "gqa_small", "k3v4_small", "k8v4_small"])
-def test_original_basis_attention_equals_decode(name):
-    w, inp, preset, lay, c, cache, _, _, kh, vh = _dequant(name)
+@pytest.mark.parametrize("name,over", [("tiny", {}), ("gqa_small", {}), ("k3v4_small", {}), ("k8v4_small", {}),
+                                       ("gqa_small", {"preset": "3bit_nc"})])
+def test_original_basis_attention_equals_decode(name, over):
+    w, inp, preset, lay, c, cache, _, _, kh, vh = _dequant(name, **over)
     q = inp.q.double().numpy()
     ref = od.decode(q, cache, lay, preset, c, inp.block_table.numpy(), inp.seq_lens.numpy())
     group = w.n_q // w.n_kv
@@ -63,9 +64,10 @@ def test_key_length_kept_by_norm_correction(name):
         assert np.max(np.abs(ratio - 1.0)) <= 2.0 ** -11 + 1e-9
 
 
-@pytest.mark.parametrize("name,bits", [("gqa_small", 4), ("k3v4_small", 3), ("long_small", 4)])
-def test_key_error_near_codebook_distortion(name, bits):
-    w, inp, _, _, _, _, ks, _, kh, _ = _dequant(name)
+@pytest.mark.parametrize("name,bits,over", [("gqa_small", 4, {}), ("k3v4_small", 3, {}), ("long_small", 4, {}),
+                                            ("gqa_small", 3, {"preset": "3bit_nc"})])
+def test_key_error_near_codebook_distortion(name, bits, over):
+    w, inp, _, _, _, _, ks, _, kh, _ = _dequant(name, **over)
     err = []
     for b in range(w.batch):
         length = int(inp.seq_lens[b])
@@ -92,15 +94,17 @@ def test_fp8_keys_are_nearest_e4m3():
         assert np.all(np.abs(got - k) <= half_ulp * (1 + 1e-12))
 
 
-@pytest.mark.parametrize("name", ["gqa_small", "k8v4_small"])
-def test_values_within_half_step(name):
-    w, inp, _, _, _, _, _, vs, _, vh = _dequant(name)
+@pytest.mark.parametrize("name,over", [("gqa_small", {}), ("k8v4_small", {}),
+                                       ("gqa_small", {"preset": "3bit_nc"})])
+def test_values_within_half_step(name, over):
+    w, inp, preset, _, _, _, _, vs, _, vh = _dequant(name, **over)
+    top = 2 ** preset.value_bits - 1
     for b in range(w.batch):
         length = int(inp.seq_lens[b])
         v = vs[b]
         mn, mx = v.min(-1, keepdims=True), v.max(-1, keepdims=True)
-        s = np.maximum((mx - mn) / 15, 1e-8)
-        tol = s / 2 * (1 + 1e-5) + 15 * s * 2.0 ** -11 + np.abs(mn) * 2.0 ** -11 + 1e-7
+        s = np.maximum((mx - mn) / top, 1e-8)
+        tol = s / 2 * (1 + 1e-5) + top * s * 2.0 ** -11 + np.abs(mn) * 2.0 ** -11 + 1e-7
         assert np.all(np.abs(vh[b, :length] - v) <= tol)
 
 

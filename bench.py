@@ -153,6 +153,19 @@ def whole_job_gbs(world: int, bytes_per_rank: int, ms: float) -> float:
     return world * bytes_per_rank / (ms * 1e-3) / 1e9
 
 
+def all_ranks_ok(ok: bool, device, world: int) -> bool:
+    """True only if ``ok`` holds on every rank (one max-reduce; every rank
+    calls it, so no rank can wait for a peer that took another branch)."""
+    return max_over_ranks([0.0 if ok else 1.0], device, world)[0] == 0.0
+
+
+def merge_timings(values, optional, device, world: int):
+    """Max over ranks of ``values`` (ms) and of ``optional`` (ms or None), in
+    one collective; the optional timing is None unless every rank has one."""
+    got = max_over_ranks(list(values) + [optional or 0.0, 1.0 if optional is None else 0.0], device, world)
+    return got[:len(values)], (None if got[-1] else got[-2])
+
+
 def _oracle_steps(workload: str, steps: int):
     """Time the oracle in a single-threaded child process (spawned, no CUDA):
     one sequence of the workload is oracle-stored once, then each step is the
@@ -304,7 +317,7 @@ def run_tq(args):
         except RuntimeError as exc:   # capture refused: only the eager steps count
             graphs, graph_note = [], "capture failed: %s" % str(exc).splitlines()[0][:120]
         # every rank times the graphs only if every rank captured them
-        if max_over_ranks([0.0 if graphs else 1.0], dev, world)[0] == 0.0:
+        if all_ranks_ok(bool(graphs), dev, world):
             for i in range(args.warmup):
                 graphs[i % n_copies].replay()
             torch.cuda.synchronize()
@@ -387,10 +400,8 @@ def run_tq(args):
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
     # ---- max over ranks
-    # one collective for every rank, whether or not its capture worked
-    step_ms, split_ms, store_ms, e2e_ms, graph_max, graph_failed = max_over_ranks(
-        [step_ms, split_ms, store_ms, e2e_ms, graph_ms or 0.0, 1.0 if graph_ms is None else 0.0], dev, world)
-    graph_ms = None if graph_failed else graph_max
+    (step_ms, split_ms, store_ms, e2e_ms), graph_ms = merge_timings([step_ms, split_ms, store_ms, e2e_ms], graph_ms,
+                                                                    dev, world)
     clocks = clk.summary()
 
     if rank == 0:

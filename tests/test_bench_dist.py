@@ -1,7 +1,8 @@
 """bench.py's multi-rank host logic on CPU: world_size 2 over gloo.
 
 Each rank is an independent replica (weak scaling, no data-path collective);
-the only exchange is the max-over-ranks of the step timings.
+the only exchanges are the max-over-ranks of the step timings and the
+agreement that every rank captured its CUDA graphs.
 """
 
 import os
@@ -42,6 +43,13 @@ def _rank_main(rank, world, port):
         mine = [1.0 + rank, 5.0 - rank, 2.0, 7.0 * (rank + 1)]
         got = bench.max_over_ranks(mine, torch.device("cpu"), world)
         assert got == [2.0, 5.0, 2.0, 14.0]
+        # CUDA-graph timing: used only if every rank captured its graphs
+        assert bench.all_ranks_ok(True, torch.device("cpu"), world)
+        assert not bench.all_ranks_ok(rank == 0, torch.device("cpu"), world)
+        vals, g = bench.merge_timings([1.0 + rank], 3.0 + rank, torch.device("cpu"), world)
+        assert vals == [2.0] and g == 4.0
+        vals, g = bench.merge_timings([1.0 + rank], None if rank == 1 else 3.0, torch.device("cpu"), world)
+        assert vals == [2.0] and g is None
         # whole-job value: all ranks' bytes over the slowest step
         assert abs(bench.whole_job_gbs(world, 140_509_184, got[0]) - 2 * 140_509_184 / 2e-3 / 1e9) < 1e-9
     finally:
@@ -58,4 +66,7 @@ def test_single_rank_needs_no_process_group():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.max_over_ranks([3.0, 4.0], torch.device("cpu"), 1) == [3.0, 4.0]
+    assert bench.merge_timings([3.0], None, torch.device("cpu"), 1) == ([3.0], None)
+    assert bench.merge_timings([3.0], 2.5, torch.device("cpu"), 1) == ([3.0], 2.5)
+    assert bench.all_ranks_ok(True, torch.device("cpu"), 1) and not bench.all_ranks_ok(False, torch.device("cpu"), 1)
     assert bench.whole_job_gbs(1, 1_000_000_000, 1000.0) == pytest.approx(1.0)

@@ -163,3 +163,14 @@ def test_dequant_argument_errors_return_before_launch(tq):
     # FP8 keys need no codebook; this call would launch, so only the argument
     # checks that come first are exercised
     assert dq(cfg_=tq.make_config("k8v4", 32, 8), cb_=None, kout=None) == _abi.TQ_ERR_INVALID_ARG
+
+
+def test_dequant_binding_rejects_mixed_output_dtypes(tq):
+    import torch
+    cfg = tq.make_config("4bit_nc", 32, 8)
+    cb = tq.tq_build_codebook(128, 4)
+    k = torch.empty((1, 16, 8, 128), dtype=torch.bfloat16)
+    v = torch.empty((1, 16, 8, 128), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        tq.tq_dequant(cfg, cb, torch.empty(16), torch.zeros((1, 1), dtype=torch.int32),
+                      torch.zeros(1, dtype=torch.int32), 16, k, v)

@@ -166,19 +166,14 @@ def merge_timings(values, optional, device, world: int):
     return got[:len(values)], (None if got[-1] else got[-2])
 
 
-def _oracle_steps(workload: str, steps: int):
-    """Time the oracle in a single-threaded child process (spawned, no CUDA):
-    one sequence of the workload is oracle-stored once, then each step is the
-    oracle store of one new token plus the oracle decode of all query heads
-    of that sequence. Returns (list of step seconds, bytes read per step)."""
-    code = f"""
+_ORACLE_STEP_SCRIPT = """
 import os, sys, time, json
-sys.path.insert(0, {ROOT!r})
-sys.path.insert(0, os.path.join({ROOT!r}, "tests"))
+sys.path.insert(0, {root!r})
+sys.path.insert(0, os.path.join({root!r}, "tests"))
 import numpy as np, workloads
 from parity import OracleCache
 from oracle import store as ost
-w = workloads.get({workload!r}, batch=1)
+w = workloads.get({workload!r}, batch=1, seed={seed})
 inp = workloads.make_inputs(w)
 oc = OracleCache(w, inp).fill()
 q = inp.q.double().numpy()
@@ -192,11 +187,40 @@ for _ in range({steps}):
     times.append(time.perf_counter() - t0)
 print(json.dumps({{"times": times, "bytes": int(inp.seq_lens.sum()) * w.n_kv * oc.lay.slot_bytes}}))
 """
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    out = subprocess.run([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE, text=True, check=True)
-    r = json.loads(out.stdout.strip().splitlines()[-1])
+
+_SINGLE_THREAD_ENV = dict(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+
+
+def _oracle_child(workload: str, steps: int, seed: int) -> subprocess.Popen:
+    code = _ORACLE_STEP_SCRIPT.format(root=ROOT, workload=workload, seed=seed, steps=steps)
+    return subprocess.Popen([sys.executable, "-c", code], env=dict(os.environ, **_SINGLE_THREAD_ENV),
+                            stdout=subprocess.PIPE, text=True)
+
+
+def _oracle_result(proc: subprocess.Popen):
+    out, _ = proc.communicate()
+    if proc.returncode != 0:
+        raise RuntimeError(f"oracle child exited {proc.returncode}")
+    r = json.loads(out.strip().splitlines()[-1])
     return r["times"], r["bytes"]
+
+
+def _oracle_steps(workload: str, steps: int):
+    """Time the oracle in a single-threaded child process (spawned, no CUDA):
+    one sequence of the workload is oracle-stored once, then each step is the
+    oracle store of one new token plus the oracle decode of all query heads
+    of that sequence. Returns (list of step seconds, bytes read per step)."""
+    return _oracle_result(_oracle_child(workload, steps, 0))
+
+
+def _oracle_steps_all_cores(workload: str, steps: int, procs: int):
+    """The same oracle step in ``procs`` single-threaded child processes at
+    once, each on a sequence of its own (seeds 0 .. procs-1). Returns the
+    aggregate bytes per second over the children's timed steps (the first two
+    steps of each are warm-up)."""
+    children = [_oracle_child(workload, steps, seed) for seed in range(procs)]
+    results = [_oracle_result(c) for c in children]
+    return sum(nbytes / statistics.mean(times[2:]) for times, nbytes in results)
 
 
 def run_reference(args):
@@ -439,6 +463,15 @@ def run_tq(args):
                 "sample": f"1 of {B} sequences ({L} tokens, {w.n_kv} KV heads, {w.n_q} query heads): "
                           "oracle store of one new token + oracle decode, mean of 6 steps after 2 warm-up",
             }
+            # the same oracle on every host core at once (one sequence per core)
+            procs = max(1, min(len(os.sched_getaffinity(0)), B))
+            try:
+                line["cpu_baseline"]["all_cores"] = {
+                    "value": _oracle_steps_all_cores(WORKLOAD, 8, procs) / 1e9, "unit": "GB/s", "cores": procs,
+                    "sample": f"{procs} sequences at once, one single-threaded process each, same steps",
+                }
+            except Exception as exc:   # a reported extra: never lose the line over it
+                line["cpu_baseline"]["all_cores"] = {"unavailable": str(exc)[:120]}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

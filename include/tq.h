@@ -23,8 +23,9 @@
  *
  * Conventions shared by every entry point
  *   - Ownership: the caller owns every buffer. The library allocates nothing,
- *     keeps no global state, never synchronises the stream and only enqueues
- *     kernels on the given stream (NULL = the legacy default stream).
+ *     keeps no global state (except the fixed device array of
+ *     tq_decode_noalloc below), never synchronises the stream and only
+ *     enqueues kernels on the given stream (NULL = the legacy default stream).
  *   - Pointers documented "device" must be CUDA device memory of the current
  *     device; "host" pointers are plain CPU memory read during the call.
  *   - Errors detectable on the host return a negative tq_status before any
@@ -240,10 +241,13 @@ tq_status tq_decode_reduce(const tq_config* cfg, const int* seq_lens, int batch,
  *   tq_decode_workspace_size(cfg, batch, max_seq_len) exceeds
  *   TQ_DECODE_NOALLOC_SCRATCH_BYTES (e.g. more than about 12,000 (sequence,
  *   KV head, partition) triples at 4 query heads per KV head).
- *   Set-up: the first call on each device (the one current at the call)
- *   looks the array's address up, which loads this part of the library on
- *   that device; make that first call before any stream capture. A failed
- *   look-up returns TQ_ERR_CUDA and is retried on the next call.
+ *   Set-up: every call looks the array's address up in the context current
+ *   on the calling thread (a host-side look-up that allocates nothing). The
+ *   first call in a context loads this part of the library there, which
+ *   places the array in that device's memory; make that first call before
+ *   any stream capture. Nothing is cached between calls, so a context that
+ *   is reset or replaced simply gets its own array on its next first call.
+ *   A failed look-up returns TQ_ERR_CUDA, launching nothing.
  *   Initial contents: nothing in the array needs to start at zero; each call
  *   writes every partial it later reads.
  *   Concurrency: all calls on one device share the one array, so two calls
@@ -281,8 +285,9 @@ tq_status tq_decode_noalloc(const tq_config* cfg, const tq_codebook* cb,
  *                 above that cap (the sequence is cut there),
  *                 TQ_DEV_BLOCK_OUT_OF_RANGE for a block id outside
  *                 [0, num_blocks) (its positions are written as 0)
- * batch == 0 or max_seq_len == 0 is a no-op. One launch, one warp per
- * (sequence, position, KV head); no workspace. */
+ * batch == 0 or max_seq_len == 0 is a no-op. One launch: a CTA per
+ * (sequence, 16-position tile, KV head), a half-warp per position; no
+ * workspace. */
 tq_status tq_dequant(const tq_config* cfg, const tq_codebook* cb,
                      const void* cache, long long num_blocks,
                      const int* block_table, int bt_stride,

@@ -17,8 +17,16 @@ import workloads
 
 @pytest.fixture(scope="module")
 def tq():
+    import os
+    import shutil
     from turboquant_paged_kv_gb300 import build
-    build.build()
+    # the host-side test below needs the library but no GPU: build it where a
+    # CUDA toolkit is present, else use an existing build, else skip
+    nvcc = os.path.exists(build.NVCC) or shutil.which("nvcc")
+    if nvcc:
+        build.build()
+    elif not os.path.exists(build.LIB_PATH):
+        pytest.skip("libtq.so is not built and no nvcc is available to build it")
     import turboquant_paged_kv_gb300 as tq
     return tq
 
@@ -106,6 +114,7 @@ def test_two_calls_in_a_row_match_tq_decode(tq, name, out_dtype):
         g = got.float().cpu().numpy()
         r = ref.float().cpu().numpy()
         assert np.all(np.isfinite(g))
-        # same kernels on the same inputs; the decode gate is 2e-3 absolute
-        np.testing.assert_allclose(g, r, rtol=0, atol=2e-3)
-        print(f"{name}: max|noalloc - tq_decode| = {np.abs(g - r).max():.2e}")
+        # the same kernels on the same inputs with the same launch shape: the
+        # results must agree bit for bit (a stale partial left in the shared
+        # array by the first call would show here)
+        assert np.array_equal(g, r), f"{name}: max|noalloc - tq_decode| = {np.abs(g - r).max():.2e}"

@@ -10,9 +10,6 @@
 // The array sits in this translation unit alone, so its module (and its
 // device memory) is only loaded by processes that call this entry point.
 
-#include <atomic>
-#include <mutex>
-
 #include <cuda_runtime.h>
 
 #include "tq.h"
@@ -21,29 +18,19 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_scratch[TQ_DECODE_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_ptr[kMaxDevices];
-std::mutex g_setup_mutex;
-
-// Address of the current device's copy of g_scratch, looked up once per
-// device (the lookup loads this module on that device).
-tq_status scratch_for_current_device(void** ptr) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TQ_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return TQ_ERR_UNSUPPORTED;
-  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
-  if (p) {
-    *ptr = p;
-    return TQ_OK;
-  }
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
-  if (!p) {
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();   // the failed lookup must not poison the caller's next check
-      return TQ_ERR_CUDA;
-    }
-    g_scratch_ptr[dev].store(p, std::memory_order_release);
+// Device address of g_scratch in the context current on the calling thread.
+// In host code the name g_scratch is only a stand-in for the symbol, never a
+// device address. The address is looked up on every call, not cached: it
+// belongs to one context and to this module's copy in it, so a cached value
+// would dangle after a context reset, or name another caller's memory when a
+// different context is current on the same device. Once the module is loaded
+// (the first call in a context does that) the look-up is a host-side table
+// read that allocates nothing.
+tq_status scratch_for_current_context(void** ptr) {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();   // the failed look-up must not poison the caller's next check
+    return TQ_ERR_CUDA;
   }
   *ptr = p;
   return TQ_OK;
@@ -63,7 +50,7 @@ extern "C" tq_status tq_decode_noalloc(const tq_config* cfg, const tq_codebook* 
                      max_seq_len, scale, out, out_dtype, nullptr, 0, dev_status, stream);
   if (need > static_cast<size_t>(TQ_DECODE_NOALLOC_SCRATCH_BYTES)) return TQ_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
-  const tq_status st = scratch_for_current_device(&scratch);
+  const tq_status st = scratch_for_current_context(&scratch);
   if (st != TQ_OK) return st;
   return tq_decode(cfg, cb, q, q_dtype, cache, num_blocks, block_table, bt_stride, seq_lens, batch, max_seq_len,
                    scale, out, out_dtype, scratch, static_cast<size_t>(TQ_DECODE_NOALLOC_SCRATCH_BYTES),

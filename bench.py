@@ -5,26 +5,36 @@ One step = the whole hot path for one decode iteration of a batch:
   write through slot_mapping) + tq_decode (rotate q, split-K attention over
   the packed cache, LSE reduce).
 
-Workload (default): batch 32 x context 4096, n_q 32, n_kv 8, d 128, block 16,
-preset 4bit_nc, bf16 inputs with one x8 outlier channel per head, block table
-a random permutation. ``value`` = logical packed-KV bytes read per step /
-step time (GB/s). Extra keys report decode tok/s, store Mtok/s (8192-token
-prefill chunk) and the split kernel's roofline.
+Workloads (``--workload``; the default is the one the headline metric is
+quoted on):
 
-L2 hygiene: three copies of the cache (3 x 143 MB, each larger than L2) are
+  gqa   batch 32 x context 4096, n_q 32, n_kv 8, 4bit_nc, bf16 inputs with one
+        x8 outlier channel per head, block table a random permutation
+  k3v4  batch 64, contexts uniform in [512, 16384], n_q 32, n_kv 8, k3v4_nc
+  k8v4  batch 128 x 8192, n_q 32, n_kv 8, k8v4 (e4m3 keys); its store line
+        is the workload's own 8192-token prefill chunk
+  long  batch 4 x 131072, n_q 64, n_kv 8, 4bit_nc, Student-t outlier channels
+  all   every workload above, one JSON line each
+
+``value`` = logical packed-KV bytes read per step / step time (GB/s). Each
+line also carries decode tok/s, the split kernel's roofline (the dominant
+kernel), the store kernel's roofline on an 8192-token prefill chunk, an
+end-to-end number through the public API with host buffers, and the CPU
+oracle timed on a bounded sample of the same workload.
+
+L2 hygiene: three copies of the cache (each larger than the 129 MB L2) are
 rotated between steps, so no step finds its cache in L2.
 
-The K timed steps are launched eagerly through the binding. The same K steps
-replayed from CUDA graphs (one captured step per cache copy, as a serving loop
-replays its decode step) are timed too and reported as ``graph_ms_per_step``
-(null, with ``config.graph`` saying why, if capture fails).
-
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
+                  [--workload gqa|k3v4|k8v4|long|all] [--partition P]
   python bench.py --op dequant [--steps K] [--warmup W]   (full dequantisation alone)
 
 ``--impl reference`` times the CPU oracle (test infrastructure) on a bounded
-sample of the same workload; N > 1 runs weak-scaling replicas (each rank its
-own batch; there is no data exchange in this path).
+sample of the same workload. N > 1 runs weak-scaling replicas, one process
+per GPU (each rank its own batch; there is no data exchange in this path):
+under torchrun the ranks come from the environment; without it bench.py
+starts the N ranks itself. ``--dry-run`` runs the multi-rank host logic on
+the CPU (gloo) without touching a GPU.
 """
 
 from __future__ import annotations
@@ -34,6 +44,7 @@ import hashlib
 import json
 import os
 import re
+import socket
 import statistics
 import subprocess
 import sys
@@ -44,7 +55,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode KV-read GB/s & % of HBM peak; decode tok/s; store Mtok/s (d=128 4bit_nc)"
-WORKLOAD = "gqa"
+WORKLOADS = ("gqa", "k3v4", "k8v4", "long")
+DEFAULT_WORKLOAD = "gqa"
+# tokens of one sequence the CPU oracle handles per step in the baseline legs
+ORACLE_SAMPLE_TOKENS = 8192
+STORE_TOKENS = 8192
 
 
 def _peaks():
@@ -56,9 +71,9 @@ def _peaks():
         return 6800.0, "fallback (6.8 TB/s)"
 
 
-def _profile_traffic(kernel_file: str, summary: str):
-    """Per-launch DRAM bytes from a committed ncu summary, if it matches the
-    current kernel source; else None."""
+def _profile_field(kernel_file: str, summary: str, field: str):
+    """A number from a committed ncu summary under profiles/, if the summary's
+    recorded source hash matches the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", summary)
     try:
         text = open(path).read()
@@ -67,10 +82,16 @@ def _profile_traffic(kernel_file: str, summary: str):
         return None
     h = hashlib.sha256(src).hexdigest()[:16]
     m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
-    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != h:
+    m_val = re.search(re.escape(field) + r":\s*([0-9.]+)", text)
+    if not m_hash or not m_val or m_hash.group(1) != h:
         return None
-    return int(m_bytes.group(1))
+    v = float(m_val.group(1))
+    return int(v) if v.is_integer() else v
+
+
+def key_bits(preset: str):
+    """Codebook bits of a preset's keys (None for e4m3 keys)."""
+    return {"4bit_nc": 4, "k3v4_nc": 3, "3bit_nc": 3}.get(preset)
 
 
 class ClockSampler:
@@ -124,6 +145,8 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ---------------------------------------------------------------- ranks
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -131,11 +154,11 @@ def _dist():
     return world, rank, local
 
 
-def rank_workload(rank: int):
+def rank_workload(rank: int, name: str = DEFAULT_WORKLOAD):
     """Rank ``rank``'s replica of the workload: same shapes, its own seed
     (weak scaling: every rank decodes a whole batch of its own)."""
     import workloads
-    return workloads.get(WORKLOAD, seed=rank)
+    return workloads.get(name, seed=rank)
 
 
 def max_over_ranks(values, device, world: int):
@@ -166,6 +189,67 @@ def merge_timings(values, optional, device, world: int):
     return got[:len(values)], (None if got[-1] else got[-2])
 
 
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_entry(rank: int, world: int, port: int, argv):
+    """One self-launched rank: the environment torchrun would give it, then
+    the ordinary entry point."""
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_WORLD_SIZE=str(world), MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    rc = main(argv)
+    if rc:
+        raise SystemExit(rc)
+
+
+def launch_ranks(n: int, argv, dry_run: bool) -> int:
+    """Start ``n`` ranks of this script (spawned processes, one per GPU) when
+    no launcher set the rank environment. Refuses, with a non-zero exit,
+    to run more ranks than there are visible GPUs."""
+    if not dry_run:
+        import torch
+        have = torch.cuda.device_count() if torch.cuda.is_available() else 0
+        if have < n:
+            print(json.dumps({"error": f"--gpus {n} needs {n} visible GPUs, found {have}"}), flush=True)
+            return 2
+    import torch.multiprocessing as mp
+    mp.start_processes(_rank_entry, args=(n, _free_port(), argv), nprocs=n, join=True, start_method="spawn")
+    return 0
+
+
+def run_dry(args) -> int:
+    """The multi-rank host logic with no GPU: process group over gloo, each
+    rank's replica workload, the max-over-ranks of (stand-in) step timings
+    and the whole-job value, printed by rank 0."""
+    import torch
+    import torch.distributed as dist
+    world, rank, _ = _dist()
+    if world > 1:
+        dist.init_process_group("gloo")
+    try:
+        import workloads
+        w = rank_workload(rank, args.workload if args.workload != "all" else DEFAULT_WORKLOAD)
+        inp = workloads.make_inputs(workloads.get(w.name + "_small", seed=w.seed)
+                                    if w.name + "_small" in workloads.WORKLOADS else w)
+        kv_bytes = int(w.batch) * (w.fixed_len or 1) * w.n_kv
+        mine = 1.0 + rank                      # stand-in step time (ms)
+        (step_ms,) = max_over_ranks([mine], torch.device("cpu"), world)
+        seeds = max_over_ranks([float(w.seed)], torch.device("cpu"), world)
+        if rank == 0:
+            print(json.dumps({"dry_run": True, "n_gpus": world, "workload": w.name, "max_step_ms": step_ms,
+                              "max_seed": seeds[0], "q_checksum_rank0": float(inp.q.float().sum()),
+                              "value": whole_job_gbs(world, kv_bytes, step_ms)}), flush=True)
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
+    return 0
+
+
+# ---------------------------------------------------------------- CPU oracle
+
 _ORACLE_STEP_SCRIPT = """
 import os, sys, time, json
 sys.path.insert(0, {root!r})
@@ -173,7 +257,13 @@ sys.path.insert(0, os.path.join({root!r}, "tests"))
 import numpy as np, workloads
 from parity import OracleCache
 from oracle import store as ost
-w = workloads.get({workload!r}, batch=1, seed={seed})
+base = workloads.get({workload!r})
+over = dict(batch=1, seed={seed}, store_tokens=0, store_extra_blocks=0)
+if base.fixed_len:
+    over["fixed_len"] = min(base.fixed_len, {cap})
+else:
+    over["len_range"] = (min(base.len_range[0], {cap}), min(base.len_range[1], {cap}))
+w = workloads.get({workload!r}, **over)
 inp = workloads.make_inputs(w)
 oc = OracleCache(w, inp).fill()
 q = inp.q.double().numpy()
@@ -185,14 +275,16 @@ for _ in range({steps}):
     ost.store(k[-1:].double().numpy(), v[-1:].double().numpy(), last, oc.cache, oc.lay, oc.preset, oc.cent, oc.mid)
     oc.decode(q)
     times.append(time.perf_counter() - t0)
-print(json.dumps({{"times": times, "bytes": int(inp.seq_lens.sum()) * w.n_kv * oc.lay.slot_bytes}}))
+print(json.dumps({{"times": times, "bytes": int(inp.seq_lens.sum()) * w.n_kv * oc.lay.slot_bytes,
+                  "tokens": int(inp.seq_lens.sum())}}))
 """
 
 _SINGLE_THREAD_ENV = dict(OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
 
 
 def _oracle_child(workload: str, steps: int, seed: int) -> subprocess.Popen:
-    code = _ORACLE_STEP_SCRIPT.format(root=ROOT, workload=workload, seed=seed, steps=steps)
+    code = _ORACLE_STEP_SCRIPT.format(root=ROOT, workload=workload, seed=seed, steps=steps,
+                                      cap=ORACLE_SAMPLE_TOKENS)
     return subprocess.Popen([sys.executable, "-c", code], env=dict(os.environ, **_SINGLE_THREAD_ENV),
                             stdout=subprocess.PIPE, text=True)
 
@@ -202,14 +294,15 @@ def _oracle_result(proc: subprocess.Popen):
     if proc.returncode != 0:
         raise RuntimeError(f"oracle child exited {proc.returncode}")
     r = json.loads(out.strip().splitlines()[-1])
-    return r["times"], r["bytes"]
+    return r["times"], r["bytes"], r["tokens"]
 
 
 def _oracle_steps(workload: str, steps: int):
     """Time the oracle in a single-threaded child process (spawned, no CUDA):
-    one sequence of the workload is oracle-stored once, then each step is the
-    oracle store of one new token plus the oracle decode of all query heads
-    of that sequence. Returns (list of step seconds, bytes read per step)."""
+    one sequence of the workload (at most ORACLE_SAMPLE_TOKENS positions) is
+    oracle-stored once, then each step is the oracle store of one new token
+    plus the oracle decode of all query heads of that sequence. Returns (list
+    of step seconds, bytes read per step, tokens of the sequence)."""
     return _oracle_result(_oracle_child(workload, steps, 0))
 
 
@@ -220,7 +313,17 @@ def _oracle_steps_all_cores(workload: str, steps: int, procs: int):
     steps of each are warm-up)."""
     children = [_oracle_child(workload, steps, seed) for seed in range(procs)]
     results = [_oracle_result(c) for c in children]
-    return sum(nbytes / statistics.mean(times[2:]) for times, nbytes in results)
+    return sum(nbytes / statistics.mean(times[2:]) for times, nbytes, _ in results)
+
+
+def _sample_text(w, tokens: int) -> str:
+    return (f"1 of {w.batch} sequences, {tokens} positions ({w.n_kv} KV heads, {w.n_q} query heads; "
+            f"sequences longer than {ORACLE_SAMPLE_TOKENS} positions are cut there): oracle store of one "
+            "new token + oracle decode")
+
+
+def _workload_text(w, extra: str = "") -> str:
+    return f"{w.name}: {w.note}, d {w.d}, block {w.block_size}, {w.preset}{extra}"
 
 
 def run_reference(args):
@@ -228,26 +331,273 @@ def run_reference(args):
     if rank != 0:
         return 0
     import workloads
-    w = workloads.get(WORKLOAD)
-    times, nbytes = _oracle_steps(WORKLOAD, args.warmup + args.steps)
-    step_s = statistics.mean(times[args.warmup:])
-    gbs = nbytes / step_s / 1e9
-    sample = (f"1 of {w.batch} sequences ({w.fixed_len} tokens, {w.n_kv} KV heads): oracle store of one new "
-              f"token + oracle decode of {w.n_q} query heads, per step")
-    line = {
-        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: {w.note}, d {w.d}, block {w.block_size}, {w.preset}"},
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
-        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-    }
-    print(json.dumps(line), flush=True)
+    for name in (WORKLOADS if args.workload == "all" else (args.workload,)):
+        w = workloads.get(name)
+        times, nbytes, tokens = _oracle_steps(name, args.warmup + args.steps)
+        step_s = statistics.mean(times[args.warmup:])
+        gbs = nbytes / step_s / 1e9
+        line = {
+            "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": _workload_text(w)},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": _sample_text(w, tokens) + ", per step"},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
     return 0
 
 
+# ---------------------------------------------------------------- GPU arm
+
+class DecodeCase:
+    """One workload's inputs, filled caches and step buffers on the device."""
+
+    def __init__(self, tq, name: str, rank: int, dev, partition: int, n_copies: int = 3):
+        import torch
+        import workloads
+        self.tq = tq
+        self.w = w = rank_workload(rank, name)
+        self.inp = inp = workloads.make_inputs(w, device=dev)
+        # seq_lens and the block table are written long before each decode (the
+        # kernel right before it is tq_store), so the split kernel may plan before
+        # waiting for that kernel
+        self.cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size, partition_tokens=partition,
+                                  flags=tq.TQ_FLAG_INDICES_READY)
+        bits = key_bits(w.preset)
+        self.cb = tq.tq_build_codebook(w.d, bits) if bits else None
+        self.lay = lay = tq.tq_layout_for(self.cfg)
+        caches = [torch.empty(inp.num_blocks * lay.block_bytes, dtype=torch.uint8, device=dev)]
+        for b in range(w.batch):   # every cached position of every sequence
+            k, v = inp.kv_for_sequence(b, dev)
+            s0 = dict(inp.fill_order)[b]
+            tq.tq_store(self.cfg, self.cb, k, v, inp.fill_slots[s0: s0 + k.shape[0]], caches[0])
+            del k, v
+        for _ in range(n_copies - 1):
+            caches.append(caches[0].clone())
+        self.caches = caches
+        torch.cuda.synchronize()
+        B = w.batch
+        self.seq_lens = inp.seq_lens
+        self.table = inp.block_table
+        self.max_len = int(inp.seq_lens.max().item())
+        last = (inp.seq_lens - 1).to(torch.int64)
+        self.last_slots = (self.table[torch.arange(B, device=dev), last // w.block_size].to(torch.int64)
+                           * w.block_size + last % w.block_size)
+        self.gen = torch.Generator(device=dev)
+        self.gen.manual_seed(1234 + rank)
+        self.new_k = torch.randn(B, w.n_kv, w.d, generator=self.gen, device=dev).to(torch.bfloat16)
+        self.new_v = torch.randn(B, w.n_kv, w.d, generator=self.gen, device=dev).to(torch.bfloat16)
+        self.q = inp.q
+        self.out = torch.empty(B, w.n_q, w.d, dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(tq.tq_decode_workspace_size(self.cfg, B, self.max_len), dtype=torch.uint8,
+                              device=dev)
+        self.kv_bytes = int(inp.seq_lens.sum().item()) * w.n_kv * lay.slot_bytes
+
+    def step(self, i):
+        tq = self.tq
+        cache = self.caches[i % len(self.caches)]
+        tq.tq_store(self.cfg, self.cb, self.new_k, self.new_v, self.last_slots, cache)
+        tq.tq_decode(self.cfg, self.cb, self.q, cache, self.table, self.seq_lens, self.max_len, self.out, self.ws)
+
+    def split_only(self, i):
+        self.tq.tq_decode_partials(self.cfg, self.cb, self.q, self.caches[i % len(self.caches)], self.table,
+                                   self.seq_lens, self.max_len, self.ws)
+
+    def store_chunk(self, dev):
+        """The store leg's inputs: the workload's own prefill chunk when it has
+        one (k8v4), else 8192 bf16 tokens through random distinct slots."""
+        import torch
+        w = self.w
+        if w.store_tokens:
+            k, v, slots = self.inp.store_chunk(dev)
+            return k, v, slots
+        k = torch.randn(STORE_TOKENS, w.n_kv, w.d, generator=self.gen, device=dev).to(torch.bfloat16)
+        v = torch.randn(STORE_TOKENS, w.n_kv, w.d, generator=self.gen, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(self.inp.num_blocks * w.block_size, generator=self.gen, device=dev)[:STORE_TOKENS]
+        return k, v, slots.to(torch.int64)
+
+
+def _events(n=2):
+    import torch
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def time_device(fn, reps: int, stream) -> float:
+    """Mean ms per call of ``fn(i)``, CUDA events on the launching stream."""
+    import torch
+    e0, e1 = _events()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(reps):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_workload(tq, name: str, args, dev, world: int, rank: int):
+    import torch
+
+    c = DecodeCase(tq, name, rank, dev, args.partition)
+    w = c.w
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        c.step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else str(dev.index or 0)
+    with ClockSampler(gpu_id) as clk:
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        step_ms = time_device(c.step, args.steps, stream)
+        if world > 1:
+            torch.distributed.barrier()
+
+        # ---- the same K steps replayed from CUDA graphs (one per cache copy),
+        # as a serving loop runs its decode step
+        graph_ms, graph_note, graphs = None, "captured", []
+        try:
+            for j in range(len(c.caches)):
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr):
+                    c.step(j)
+                graphs.append(gr)
+        except RuntimeError as exc:   # capture refused: only the eager steps count
+            graphs, graph_note = [], "capture failed: %s" % str(exc).splitlines()[0][:120]
+        if all_ranks_ok(bool(graphs), dev, world):
+            for i in range(args.warmup):
+                graphs[i % len(graphs)].replay()
+            graph_ms = time_device(lambda i: graphs[i % len(graphs)].replay(), args.steps, stream)
+        elif graphs:
+            graph_note = "capture failed on another rank"
+        del graphs
+
+        # ---- split kernel alone (the dominant kernel), same stream, rotated caches
+        for i in range(3):
+            c.split_only(i)
+        split_ms = time_device(c.split_only, max(args.steps, 100), stream)
+
+    # ---- store throughput on a prefill chunk
+    st_k, st_v, st_slots = c.store_chunk(dev)
+    scratch = c.caches[1]
+    n_store = st_k.shape[0]
+
+    def store_once(_i):
+        tq.tq_store(c.cfg, c.cb, st_k, st_v, st_slots, scratch)
+
+    for i in range(3):
+        store_once(i)
+    store_ms = time_device(store_once, 200, stream)
+
+    # ---- end to end through the public API with host buffers. Every step
+    # copies its inputs (packed in one pinned buffer, 256-byte aligned parts)
+    # host -> device, runs store + decode and copies the output back, and the
+    # host waits for that output before the next step, as a serving loop that
+    # samples the next token does. Timed on the host clock.
+    parts = [c.q, c.new_k, c.new_v, c.last_slots, c.seq_lens, c.table]
+    offs, total = [], 0
+    for t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    pack_h = torch.empty(total, dtype=torch.uint8).pin_memory()
+    pack_d = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def view(buf, t, off):
+        return buf[off: off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+
+    for t, off in zip(parts, offs):
+        view(pack_h, t, off).copy_(t.cpu())
+    q_d, nk_d, nv_d, sl_d, lens_d, tab_d = (view(pack_d, t, off) for t, off in zip(parts, offs))
+    out_h = torch.empty(c.out.shape, dtype=c.out.dtype).pin_memory()
+    h2d = total
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step(i):
+        pack_d.copy_(pack_h, non_blocking=True)
+        cache = c.caches[i % len(c.caches)]
+        tq.tq_store(c.cfg, c.cb, nk_d, nv_d, sl_d, cache)
+        tq.tq_decode(c.cfg, c.cb, q_d, cache, tab_d, lens_d, c.max_len, c.out, c.ws)
+        out_h.copy_(c.out, non_blocking=True)
+        stream.synchronize()   # the host reads this step's output
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+
+    # ---- max over ranks
+    (step_ms, split_ms, store_ms, e2e_ms), graph_ms = merge_timings([step_ms, split_ms, store_ms, e2e_ms], graph_ms,
+                                                                    dev, world)
+    clocks = clk.summary()
+    if rank != 0:
+        return None
+    peak, peak_src = _peaks()
+    gbs = whole_job_gbs(world, c.kv_bytes, step_ms)
+    split_gbs = c.kv_bytes / (split_ms * 1e-3) / 1e9
+    store_bytes = n_store * (w.n_kv * (2 * w.d * 2 + c.lay.slot_bytes) + 8)
+    store_gbs = store_bytes / (store_ms * 1e-3) / 1e9
+    split_note = ("stream-K: equal slice ranges per CTA" if args.partition == 0
+                  else f"fixed partitions of {args.partition} positions")
+    line = {
+        "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 mma / f32 accumulate over %s codes" % ("e4m3 key" if w.preset == "k8v4" else
+                                                             "%d-bit key" % key_bits(w.preset)),
+        "data": "synthetic",
+        "config": {"workload": _workload_text(w, ", bf16 in/out"),
+                   "partition_tokens": args.partition, "split": split_note,
+                   "l2": "%d rotated cache copies of %.0f MB each (> L2)" % (len(c.caches), c.caches[0].numel() / 1e6),
+                   "kv_bytes_per_step": c.kv_bytes, "graph": graph_note},
+        "graph_ms_per_step": graph_ms,
+        "decode_tok_s": world * w.batch / (step_ms * 1e-3),
+        "hbm_frac_step": gbs / world / peak,
+        "store_mtok_s": n_store / (store_ms * 1e-3) / 1e6,
+        "roofline": {"kernel": "split_kernel (tq_decode_partials)", "bound": "hbm", "achieved": split_gbs,
+                     "peak": peak, "unit": "GB/s", "frac": split_gbs / peak,
+                     "traffic": _profile_field("tq_decode.cu", f"decode_split_{name}.md", "dram_bytes_per_launch"),
+                     "peak_source": peak_src, "ms_per_launch": split_ms,
+                     "algorithmic_bytes_per_launch": c.kv_bytes},
+        "store_roofline": {"kernel": "store_kernel (tq_store), %d-token prefill chunk" % n_store, "bound": "hbm",
+                           "achieved": store_gbs, "peak": peak, "unit": "GB/s", "frac": store_gbs / peak,
+                           "issue_frac": _profile_field("tq_store.cu", f"store_{name}.md", "issue_active_frac"),
+                           "traffic": _profile_field("tq_store.cu", f"store_{name}.md", "dram_bytes_per_launch"),
+                           "peak_source": peak_src, "ms_per_launch": store_ms,
+                           "algorithmic_bytes_per_launch": store_bytes, "mtok_s": n_store / (store_ms * 1e-3) / 1e6},
+        "e2e": {"value": whole_job_gbs(world, c.kv_bytes, e2e_ms), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "timing": "host clock; each step ends when the host has the step's output"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        times, nbytes, tokens = _oracle_steps(name, 8)
+        step_s = statistics.mean(times[2:])
+        line["cpu_baseline"] = {
+            "value": nbytes / step_s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": _sample_text(w, tokens) + ", mean of 6 steps after 2 warm-up",
+        }
+        procs = max(1, min(len(os.sched_getaffinity(0)), w.batch))
+        try:
+            line["cpu_baseline"]["all_cores"] = {
+                "value": _oracle_steps_all_cores(name, 8, procs) / 1e9, "unit": "GB/s", "cores": procs,
+                "sample": f"{procs} sequences at once, one single-threaded process each, same steps",
+            }
+        except Exception as exc:   # a reported extra: never lose the line over it
+            line["cpu_baseline"]["all_cores"] = {"unavailable": str(exc)[:120]}
+    return line
+
+
 def run_tq(args):
-    import numpy as np
     import torch
 
     world, rank, local = _dist()
@@ -264,215 +614,12 @@ def run_tq(args):
     if world > 1:
         torch.distributed.barrier()
     import turboquant_paged_kv_gb300 as tq
-    import workloads
 
-    w = rank_workload(rank)
-    inp = workloads.make_inputs(w, device=dev)
-    # seq_lens and the block table are written long before each decode (the
-    # kernel right before it is tq_store), so the split kernel may plan before
-    # waiting for that kernel
-    cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size, partition_tokens=args.partition,
-                         flags=tq.TQ_FLAG_INDICES_READY)
-    cb = tq.tq_build_codebook(w.d, 4)
-    lay = tq.tq_layout_for(cfg)
-    n_copies = 3
-    caches = [torch.empty(inp.num_blocks * lay.block_bytes, dtype=torch.uint8, device=dev)]
-    # fill the cache: every cached position of every sequence
-    for b in range(w.batch):
-        k, v = inp.kv_for_sequence(b, dev)
-        s0 = dict(inp.fill_order)[b]
-        tq.tq_store(cfg, cb, k, v, inp.fill_slots[s0: s0 + k.shape[0]], caches[0])
-    for _ in range(n_copies - 1):
-        caches.append(caches[0].clone())
-    torch.cuda.synchronize()
-
-    B, L = w.batch, w.fixed_len
-    seq_lens = inp.seq_lens
-    table = inp.block_table
-    max_len = int(seq_lens.max().item())
-    last_slots = table[torch.arange(B, device=dev), (seq_lens - 1) // w.block_size].to(torch.int64) * w.block_size \
-        + ((seq_lens - 1) % w.block_size).to(torch.int64)
-    g = torch.Generator(device=dev)
-    g.manual_seed(1234 + rank)
-    new_k = torch.randn(B, w.n_kv, w.d, generator=g, device=dev).to(torch.bfloat16)
-    new_v = torch.randn(B, w.n_kv, w.d, generator=g, device=dev).to(torch.bfloat16)
-    q = inp.q
-    out = torch.empty(B, w.n_q, w.d, dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(tq.tq_decode_workspace_size(cfg, B, max_len), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-    kv_bytes = int(seq_lens.sum().item()) * w.n_kv * lay.slot_bytes
-
-    def step(i):
-        cache = caches[i % n_copies]
-        tq.tq_store(cfg, cb, new_k, new_v, last_slots, cache)
-        tq.tq_decode(cfg, cb, q, cache, table, seq_lens, max_len, out, ws)
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    props = torch.cuda.get_device_properties(dev)
-    gpu_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else str(dev.index or 0)
-    with ClockSampler(gpu_id) as clk:
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        ev0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        eager_ms = ev0.elapsed_time(ev1) / args.steps
-
-        # ---- the same K steps replayed from CUDA graphs (one per cache copy),
-        # as a serving loop runs its decode step
-        graph_ms, graph_note, graphs = None, "captured", []
-        try:
-            for c in range(n_copies):
-                gr = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gr):
-                    step(c)
-                graphs.append(gr)
-        except RuntimeError as exc:   # capture refused: only the eager steps count
-            graphs, graph_note = [], "capture failed: %s" % str(exc).splitlines()[0][:120]
-        # every rank times the graphs only if every rank captured them
-        if all_ranks_ok(bool(graphs), dev, world):
-            for i in range(args.warmup):
-                graphs[i % n_copies].replay()
-            torch.cuda.synchronize()
-            if world > 1:
-                torch.distributed.barrier()
-            ev0.record(stream)
-            for i in range(args.steps):
-                graphs[i % n_copies].replay()
-            ev1.record(stream)
-            torch.cuda.synchronize()
-            if world > 1:
-                torch.distributed.barrier()
-            graph_ms = ev0.elapsed_time(ev1) / args.steps
-        elif graphs:
-            graph_note = "capture failed on another rank"
-        step_ms = eager_ms
-
-        # ---- split kernel alone (the dominant kernel), same stream, rotated caches
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = max(args.steps, 20)
-        e0.record(stream)
-        for i in range(reps):
-            tq.tq_decode_partials(cfg, cb, q, caches[i % n_copies], table, seq_lens, max_len, ws)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        split_ms = e0.elapsed_time(e1) / reps
-
-    # ---- store throughput on an 8192-token prefill chunk (random distinct slots)
-    n_store = 8192
-    st_k = torch.randn(n_store, w.n_kv, w.d, generator=g, device=dev).to(torch.bfloat16)
-    st_v = torch.randn(n_store, w.n_kv, w.d, generator=g, device=dev).to(torch.bfloat16)
-    st_slots = torch.randperm(inp.num_blocks * w.block_size, generator=g, device=dev)[:n_store].to(torch.int64)
-    scratch = caches[1]
-    for _ in range(3):
-        tq.tq_store(cfg, cb, st_k, st_v, st_slots, scratch)
-    e0.record(stream)
-    st_reps = 50
-    for _ in range(st_reps):
-        tq.tq_store(cfg, cb, st_k, st_v, st_slots, scratch)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    store_ms = e0.elapsed_time(e1) / st_reps
-
-    # ---- end to end through the public API with host buffers
-    # the step's inputs packed into one pinned host buffer and one device
-    # buffer (each part 256-byte aligned): one host->device copy per step
-    parts = [q, new_k, new_v, last_slots, seq_lens, table]
-    offs, total = [], 0
-    for t in parts:
-        offs.append(total)
-        total += (t.numel() * t.element_size() + 255) // 256 * 256
-    pack_h = torch.empty(total, dtype=torch.uint8).pin_memory()
-    pack_d = torch.empty(total, dtype=torch.uint8, device=dev)
-
-    def view(buf, t, off):
-        return buf[off: off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-
-    for t, off in zip(parts, offs):
-        view(pack_h, t, off).copy_(t.cpu())
-    q_d, nk_d, nv_d, sl_d, lens_d, tab_d = (view(pack_d, t, off) for t, off in zip(parts, offs))
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = total
-    d2h = out_h.numel() * out_h.element_size()
-
-    def e2e_step(i):
-        pack_d.copy_(pack_h, non_blocking=True)
-        cache = caches[i % n_copies]
-        tq.tq_store(cfg, cb, nk_d, nv_d, sl_d, cache)
-        tq.tq_decode(cfg, cb, q_d, cache, tab_d, lens_d, max_len, out, ws)
-        out_h.copy_(out, non_blocking=True)
-
-    for i in range(args.warmup):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-
-    # ---- max over ranks
-    (step_ms, split_ms, store_ms, e2e_ms), graph_ms = merge_timings([step_ms, split_ms, store_ms, e2e_ms], graph_ms,
-                                                                    dev, world)
-    clocks = clk.summary()
-
-    if rank == 0:
-        peak, peak_src = _peaks()
-        gbs = whole_job_gbs(world, kv_bytes, step_ms)
-        split_gbs = kv_bytes / (split_ms * 1e-3) / 1e9
-        line = {
-            "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16 mma / f32 accumulate over 4-bit codes", "data": "synthetic",
-            "config": {"workload": f"{WORKLOAD}: {w.note}, d {w.d}, block {w.block_size}, {w.preset}, bf16 in/out",
-                       "partition_tokens": args.partition, "split": "stream-K: equal tile ranges per warp" if args.partition == 0 else "fixed partitions",
-                       "l2": "3 rotated cache copies of %.0f MB each (> L2)" % (caches[0].numel() / 1e6),
-                       "kv_bytes_per_step": kv_bytes, "graph": graph_note},
-            "graph_ms_per_step": graph_ms,
-            "decode_tok_s": world * B / (step_ms * 1e-3),
-            "hbm_frac_step": gbs / world / peak,
-            "store_mtok_s": n_store / (store_ms * 1e-3) / 1e6,
-            "store_gbs": n_store * (w.n_kv * (2 * w.d * 2 + lay.slot_bytes) + 8) / (store_ms * 1e-3) / 1e9,
-            "roofline": {"kernel": "split_kernel (tq_decode_partials)", "bound": "hbm", "achieved": split_gbs,
-                         "peak": peak, "unit": "GB/s", "frac": split_gbs / peak,
-                         "traffic": _profile_traffic("tq_decode.cu", "decode_split_gqa.md"),
-                         "peak_source": peak_src, "ms_per_launch": split_ms,
-                         "algorithmic_bytes_per_launch": kv_bytes},
-            "e2e": {"value": whole_job_gbs(world, kv_bytes, e2e_ms), "unit": "GB/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": 3 * args.steps,
-            "clocks": clocks,
-        }
-        if not args.no_cpu_baseline:
-            times, nbytes = _oracle_steps(WORKLOAD, 8)
-            step_s = statistics.mean(times[2:])
-            line["cpu_baseline"] = {
-                "value": nbytes / step_s / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                "sample": f"1 of {B} sequences ({L} tokens, {w.n_kv} KV heads, {w.n_q} query heads): "
-                          "oracle store of one new token + oracle decode, mean of 6 steps after 2 warm-up",
-            }
-            # the same oracle on every host core at once (one sequence per core)
-            procs = max(1, min(len(os.sched_getaffinity(0)), B))
-            try:
-                line["cpu_baseline"]["all_cores"] = {
-                    "value": _oracle_steps_all_cores(WORKLOAD, 8, procs) / 1e9, "unit": "GB/s", "cores": procs,
-                    "sample": f"{procs} sequences at once, one single-threaded process each, same steps",
-                }
-            except Exception as exc:   # a reported extra: never lose the line over it
-                line["cpu_baseline"]["all_cores"] = {"unavailable": str(exc)[:120]}
-        print(json.dumps(line), flush=True)
+    for name in (WORKLOADS if args.workload == "all" else (args.workload,)):
+        line = run_workload(tq, name, args, dev, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        torch.cuda.empty_cache()
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
@@ -494,7 +641,7 @@ def run_dequant(args):
     import turboquant_paged_kv_gb300 as tq
     import workloads
 
-    w = workloads.get(WORKLOAD)
+    w = workloads.get(DEFAULT_WORKLOAD)
     inp = workloads.make_inputs(w, device=dev)
     cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size)
     cb = tq.tq_build_codebook(w.d, 4)
@@ -512,53 +659,64 @@ def run_dequant(args):
     nbytes = positions * (lay.slot_bytes + 2 * w.d * 2)    # packed slot in, bf16 key + value out
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step(_i=0):
         tq.tq_dequant(cfg, cb, cache, inp.block_table, inp.seq_lens, max_len, k_out, v_out)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     props = torch.cuda.get_device_properties(dev)
     gpu_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else "0"
     with ClockSampler(gpu_id) as clk:
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
+        ms = time_device(step, max(args.steps, 50), stream)
     peak, peak_src = _peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
     print(json.dumps({
         "op": "dequant", "metric": "full dequant GB/s (packed slots read + bf16 K/V written)",
-        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": max(args.steps, 50), "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "dtype": "f32 arithmetic, bf16 out", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: {w.note}, d {w.d}, block {w.block_size}, {w.preset}, bf16 out",
+        "config": {"workload": _workload_text(w, ", bf16 out"),
                    "l2": "each launch moves %.0f MB (> L2)" % (nbytes / 1e6), "bytes_per_launch": nbytes},
         "roofline": {"kernel": "dequant_kernel (tq_dequant)", "bound": "hbm", "achieved": gbs, "peak": peak,
                      "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src, "ms_per_launch": ms,
+                     "traffic": _profile_field("tq_dequant.cu", "dequant_gqa.md", "dram_bytes_per_launch"),
                      "algorithmic_bytes_per_launch": nbytes},
-        "gpu_launches": args.steps,
+        "gpu_launches": max(args.steps, 50),
         "clocks": clk.summary(),
     }), flush=True)
     return 0
 
 
-def main():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=WORKLOADS + ("all",))
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dry-run", action="store_true",
+                    help="run the multi-rank host logic on the CPU (gloo) without a GPU")
     ap.add_argument("--op", default="decode", choices=["decode", "dequant"],
                     help="decode: the decode step (default); dequant: tq_dequant of the gqa cache alone")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    return args
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
+    args = parse_args(argv)
+    world, _, _ = _dist()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return launch_ranks(args.gpus, argv, args.dry_run)
+    if "WORLD_SIZE" in os.environ and args.gpus != world:
+        print(json.dumps({"error": f"--gpus {args.gpus} but the launcher started {world} ranks"}), flush=True)
+        return 2
+    if args.dry_run:
+        return run_dry(args)
     if args.op == "dequant":
         return run_dequant(args)
     return run_reference(args) if args.impl == "reference" else run_tq(args)

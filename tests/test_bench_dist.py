@@ -70,3 +70,33 @@ def test_single_rank_needs_no_process_group():
     assert bench.merge_timings([3.0], 2.5, torch.device("cpu"), 1) == ([3.0], 2.5)
     assert bench.all_ranks_ok(True, torch.device("cpu"), 1) and not bench.all_ranks_ok(False, torch.device("cpu"), 1)
     assert bench.whole_job_gbs(1, 1_000_000_000, 1000.0) == pytest.approx(1.0)
+
+
+def _bench(*args, timeout=300):
+    import json
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    proc = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT, env=env,
+                          stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, timeout=timeout)
+    lines = [json.loads(x) for x in proc.stdout.splitlines() if x.startswith("{")]
+    return proc.returncode, lines, proc.stderr
+
+
+def test_gpus_flag_self_launches_ranks():
+    # no launcher: `bench.py --gpus 2` starts the two ranks itself; the dry run
+    # takes the multi-rank host path (gloo) and rank 0 alone prints the line
+    rc, lines, err = _bench("--gpus", "2", "--dry-run")
+    assert rc == 0, err
+    assert len(lines) == 1
+    line = lines[0]
+    assert line["dry_run"] and line["n_gpus"] == 2
+    assert line["max_step_ms"] == 2.0      # max over ranks of 1 + rank
+    assert line["max_seed"] == 1.0         # rank 1 drew its own replica
+
+
+def test_gpus_flag_refuses_more_ranks_than_gpus():
+    rc, lines, _ = _bench("--gpus", "2")
+    assert rc == 2
+    assert lines and "needs 2 visible GPUs" in lines[0]["error"]

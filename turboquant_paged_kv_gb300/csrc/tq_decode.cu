@@ -22,8 +22,12 @@
 //  segment + warp, which is unique because both sequences are monotone. Every
 //  warp does the same amount of work whatever the sequence lengths are.
 //
-//  Data movement. One CTA per SM: a producer warp and up to 11 consumer
-//  warps (3 warps per sub-partition). Producer lane j walks consumer j's range
+//  Data movement. One CTA per SM: two producer warps and up to 10 consumer
+//  warps (3 warps per sub-partition); producer p feeds consumers p, p + 2, ...,
+//  so each producer's pass issues the copies of half the consumers (one
+//  producer serving all of them was the kernel's limit: each bulk copy issue
+//  costs ~95 cycles and a pass served 11 lanes one after another). The lane of
+//  a producer that feeds consumer j walks consumer j's range
 //  chunk by chunk (a chunk is up to 2 consecutive tiles of one segment), loads
 //  the next chunk's block ids while the current one is issued (read one pass
 //  later, so the load latency overlaps other lanes' work), and fills consumer
@@ -93,9 +97,13 @@ namespace {
 
 constexpr int kD = 128;
 #ifndef TQ_DECODE_WARPS
-#define TQ_DECODE_WARPS 11
+#define TQ_DECODE_WARPS 10
 #endif
 constexpr int kMaxConsumers = TQ_DECODE_WARPS;   // consumer warps per CTA (fewer when shared memory is short)
+#ifndef TQ_PRODUCER_WARPS
+#define TQ_PRODUCER_WARPS 2
+#endif
+constexpr int kProducers = TQ_PRODUCER_WARPS;   // producer warps; producer p feeds consumers p, p + kProducers, ...
 #ifndef TQ_DECODE_CHUNK
 #define TQ_DECODE_CHUNK 2
 #endif
@@ -111,16 +119,13 @@ constexpr int kMaxConsumers = TQ_DECODE_WARPS;   // consumer warps per CTA (fewe
 constexpr int kChunk = TQ_DECODE_CHUNK;     // tiles per ring stage
 constexpr int kStages = TQ_DECODE_STAGES;   // ring stages per consumer warp
 constexpr float kTau = 8.0f;            // lazy rescale threshold, log2 units
-constexpr uint32_t kWaitLimit = 1u << 16;
-#ifndef TQ_SUSPEND_NS
-#define TQ_SUSPEND_NS 20000
-#endif
-constexpr uint32_t kSuspendNs = TQ_SUSPEND_NS;  // try_wait suspend hint: bound ~ kWaitLimit * hint
-constexpr int kProducerSpin = 1 << 21;  // producer polls without progress before it gives up
+constexpr uint64_t kWaitNs = 20000000;  // every wait gives up after 20 ms without progress
+constexpr uint32_t kSuspendNs = 1000;     // try_wait suspend-time hint
 constexpr int kMaxCtas = 256;           // grid cap; sizes the workspace without a device query
 constexpr int kRecordWarps = 16;        // consumer warps per CTA the workspace allows for
 static_assert(kMaxConsumers <= kRecordWarps, "workspace sized for at most 16 consumer warps per CTA");
-static_assert(kMaxConsumers <= 32, "one producer lane per consumer warp");
+static_assert(kMaxConsumers <= 32 * kProducers, "one producer lane per consumer warp");
+static_assert(kMaxConsumers + kProducers <= 12, "12 warps keep 168 registers per thread");
 // Shared-memory head: mbarriers (full and empty per (consumer, stage), then one
 // "q empty" per consumer) in the first kBarHead bytes, then one query slot of
 // G * d * 2 bytes per consumer.
@@ -224,10 +229,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait; returns false when the limit expired.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+// Bounded wait for the phase of parity `parity`: returns false once kWaitNs
+// have passed without it completing.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  do {
     if (mbar_try(bar, parity)) return true;
+  } while (global_ns() - t0 < kWaitNs);
   return false;
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
@@ -297,10 +311,11 @@ __device__ __forceinline__ void fwht128(float v[4], int lane) {
 
 // *p if pred, else dflt: a predicated load into a preset register, so nothing
 // consumes the loaded value here and the warp does not wait for it (a select
-// on the loaded value would); the address is not touched when !pred.
+// on the loaded value would); the address is not touched when !pred. L2 only,
+// like every load of data another kernel may write (tq_launch.cuh).
 __device__ __forceinline__ int ldg_or(const int* p, bool pred, int dflt) {
   int v = dflt;
-  asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q ld.global.nc.b32 %0, [%1];\n}\n"
+  asm volatile("{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q ld.global.cg.b32 %0, [%1];\n}\n"
                : "+r"(v)
                : "l"(p), "r"(static_cast<unsigned>(pred)));
   return v;
@@ -413,7 +428,7 @@ __device__ __forceinline__ void cursor_next(Cursor& u, const DecodeArgs& a) {
   u.h = 0;
   do {
     ++u.b;
-    u.len = clamp_len(a, __ldg(a.seq_lens + u.b));
+    u.len = clamp_len(a, ld_dep_s32(a.seq_lens + u.b));
     u.nt = (u.len + kTileTokens - 1) / kTileTokens;
   } while (u.nt == 0);
 }
@@ -428,7 +443,7 @@ __device__ __forceinline__ void cursor_next(Cursor& u, const DecodeArgs& a) {
 // "q empty" barrier). A consumer whose range is empty gets one descriptor with
 // n = 0 and the last bit. The block ids of the next chunk are loaded when the
 // current one is issued, so their latency overlaps the wait for a free stage.
-__device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_t qslots, uint32_t first,
+__device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, uint32_t qslots, uint32_t first,
                               uint32_t lut, uint32_t klut) {
   // Everything that may read what the previous kernel wrote comes after
   // grid_dep_wait(); with early_indices the lengths and block ids are not
@@ -440,9 +455,10 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
   };
   if (!a.early_indices) wait_previous();
   const int lane = threadIdx.x & 31;
-  const bool mine = lane < W;
+  const int jc = lane * kProducers + p;   // the consumer warp this lane feeds
+  const bool mine = jc < W;
   const long long nw = static_cast<long long>(gridDim.x) * W;
-  const long long wid = static_cast<long long>(blockIdx.x) * W + lane;
+  const long long wid = static_cast<long long>(blockIdx.x) * W + jc;
 
   // the block table is read block id by block id below: start it towards L2
   // now, spread over the grid (at most 16 MB of table)
@@ -462,7 +478,7 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
     const int j = b0 + lane;
     int nt = 0;
     if (j < a.batch) {
-      const int raw = __ldg(a.seq_lens + j);
+      const int raw = ld_dep_s32(a.seq_lens + j);
       too_long |= raw > min(a.max_seq_len, a.cap);
       const int len = clamp_len(a, raw);
       if (b0 == 0) len0 = len;
@@ -491,7 +507,7 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
     long long acc = 0;   // tiles before the group
     for (int b0 = 0; b0 < a.batch && __any_sync(0xffffffffu, !found); b0 += 32) {
       const int bb = b0 + lane;
-      const int len = bb < a.batch ? (b0 == 0 ? len0 : clamp_len(a, __ldg(a.seq_lens + bb))) : 0;
+      const int len = bb < a.batch ? (b0 == 0 ? len0 : clamp_len(a, ld_dep_s32(a.seq_lens + bb))) : 0;
       const int nt = (len + kTileTokens - 1) / kTileTokens;
       const long long span = static_cast<long long>(nt) * a.n_kv;
       long long inc = span;
@@ -558,14 +574,14 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
   // stage_at without its division: stages [0, nb_front) lie before the LUT
   const uint32_t nb_front = klut && lut > first ? (lut - first) / a.stage_bytes : (klut ? 0u : 0xFFFFFFFFu);
   const uint32_t back = lut + klut;
-  const uint32_t qslot = qslots + static_cast<uint32_t>(mine ? lane : 0) * a.qbuf_bytes;
-  const uint32_t qbar = q_empty_bar(bars, W, mine ? lane : 0);
+  const uint32_t qslot = qslots + static_cast<uint32_t>(mine ? jc : 0) * a.qbuf_bytes;
+  const uint32_t qbar = q_empty_bar(bars, W, mine ? jc : 0);
   uint32_t eparity = (1u << kStages) - 1;   // empty-barrier parity to wait for, per stage
   uint32_t used = 0, fpar = 0;              // stages ever filled; parity of their next fill
   int ps = 0, prev_seg = -1;
   int qn = 0, qdone = 0;                    // query copies issued / known consumed
   bool done = !mine;
-  int idle = 0;
+  uint64_t idle_since = 0;   // start of the current stretch without progress (0: none)
   while (__any_sync(0xffffffffu, !done)) {
     bool progressed = false;
     // one chunk per lane per pass: the block ids plan() loads for the next
@@ -576,10 +592,10 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
         if (!mbar_test(qbar, (qn - 1) & 1)) break;
         qdone = qn;
       }
-      const uint32_t fb = full_bar(bars, lane, ps);
+      const uint32_t fb = full_bar(bars, jc, ps);
       if (!mbar_test(fb + 8, (eparity >> ps) & 1u)) break;
       eparity ^= 1u << ps;
-      const uint32_t idx = static_cast<uint32_t>(lane * kStages + ps);
+      const uint32_t idx = static_cast<uint32_t>(jc * kStages + ps);
       const uint32_t sa = idx < nb_front ? first + idx * a.stage_bytes : back + (idx - nb_front) * a.stage_bytes;
       const bool last = rem <= 0;
       uint32_t okm = 0, bytes = 0;
@@ -622,18 +638,21 @@ __device__ void producer_warp(const DecodeArgs& a, int W, uint32_t bars, uint32_
       else plan();
     }
     if (__any_sync(0xffffffffu, progressed)) {
-      idle = 0;
-    } else if (++idle > kProducerSpin) {   // a consumer stopped taking stages
-      if (lane == 0) flag(a.status, TQ_DEV_TIMEOUT);
-      break;
+      idle_since = 0;
     } else {
+      const uint64_t now = global_ns();
+      if (!idle_since) idle_since = now;
+      else if (now - idle_since > kWaitNs) {   // a consumer stopped taking stages
+        if (lane == 0) flag(a.status, TQ_DEV_TIMEOUT);
+        break;
+      }
       if (TQ_PRODUCER_SLEEP_NS > 0) __nanosleep(TQ_PRODUCER_SLEEP_NS);
     }
   }
   // every copy this lane issued has landed before the warp leaves (bounded)
   if (mine)
     for (int s = 0; s < kStages; ++s)
-      if ((used >> s) & 1u) mbar_wait(full_bar(bars, lane, s), ((fpar >> s) & 1u) ^ 1u);
+      if ((used >> s) & 1u) mbar_wait(full_bar(bars, jc, s), ((fpar >> s) & 1u) ^ 1u);
 }
 
 // ---------------------------------------------------------------- consumer warps
@@ -1063,13 +1082,14 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
 
 // ---------------------------------------------------------------- split kernel
 
-// Warp 0 is the producer; warps 1 .. W are consumers. One CTA per SM.
+// Warps 0 .. kProducers - 1 are producers; the rest are the W consumers. One
+// CTA per SM.
 template <int KMODE, int GBIG, typename TQ>
-__global__ void __launch_bounds__((kMaxConsumers + 1) * 32, 1)
+__global__ void __launch_bounds__((kMaxConsumers + kProducers) * 32, 1)
 split_kernel(const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t s_dyn[];
   const int warp = threadIdx.x >> 5;
-  const int W = static_cast<int>(blockDim.x >> 5) - 1;
+  const int W = static_cast<int>(blockDim.x >> 5) - kProducers;
   const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(s_dyn));
   const uint32_t end = base + static_cast<uint32_t>(a.dyn_bytes);
   constexpr uint32_t kLut = lut_bytes<KMODE>();
@@ -1090,18 +1110,22 @@ split_kernel(const DecodeArgs a) {
   // grid_dep_wait() may read what that kernel wrote. The producer starts as
   // soon as the barriers exist; the consumers build the LUT meanwhile and meet
   // it on named barrier 1 (arrive / sync).
-  if (warp == 0) {
-    const int lane = threadIdx.x & 31;
-    for (int i = lane; i < 2 * W * kStages + W; i += 32) mbar_init(bars + 8 * i, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    __syncwarp();
-    producer_warp(a, W, bars, qslots, first, lut, kLut);   // waits for the previous kernel itself
+  if (warp < kProducers) {
+    if (warp == 0) {
+      const int lane = threadIdx.x & 31;
+      for (int i = lane; i < 2 * W * kStages + W; i += 32) mbar_init(bars + 8 * i, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (kProducers > 1) asm volatile("bar.sync 2, %0;\n" ::"r"(kProducers * 32) : "memory");   // barriers exist
+    else __syncwarp();
+    producer_warp(a, W, warp, bars, qslots, first, lut, kLut);   // waits for the previous kernel itself
   } else {
-    if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent, threadIdx.x - 32, blockDim.x - 32);
+    constexpr int kP = kProducers * 32;
+    if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent, threadIdx.x - kP, blockDim.x - kP);
     asm volatile("bar.sync 1, %0;\n" ::"r"(blockDim.x) : "memory");
-    grid_dep_wait();   // already resolved: the producer passed it before arriving
+    grid_dep_wait();   // already resolved: the producers passed it before arriving
     grid_dep_launch();
-    consumer_warp<KMODE, GBIG, TQ>(a, W, warp - 1, bars, qslots, first, lut, kLut);
+    consumer_warp<KMODE, GBIG, TQ>(a, W, warp - kProducers, bars, qslots, first, lut, kLut);
   }
 }
 
@@ -1115,7 +1139,7 @@ __device__ __forceinline__ void store_out(void* out, long long i, float v) {
 }
 
 __device__ __forceinline__ int reduce_len(const ReduceArgs& a, int b) {
-  return min(max(__ldg(a.seq_lens + b), 0), min(a.max_seq_len, a.cap));
+  return min(max(ld_dep_s32(a.seq_lens + b), 0), min(a.max_seq_len, a.cap));
 }
 
 // The reduce. The records of a partition are those of the consumer warps
@@ -1262,12 +1286,12 @@ __global__ void __launch_bounds__(8 * kD) reduce_bh_kernel(const ReduceArgs a) {
       float x[kCand];    // this thread's coordinate of every candidate's partial
 #pragma unroll
       for (int i = 0; i < kCand; ++i)
-        x[i] = i < cnt ? a.rec_o[(static_cast<long long>(s_rec[i]) * G + gg) * kD + d] : 0.f;
+        x[i] = i < cnt ? ld_dep_f32(a.rec_o + (static_cast<long long>(s_rec[i]) * G + gg) * kD + d) : 0.f;
       if (w0) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           if (k < G) {
-            const float lse = ok ? a.rec_lse[rec * G + k] : -INFINITY;
+            const float lse = ok ? ld_dep_f32(a.rec_lse + rec * G + k) : -INFINITY;
             float cm = lse;
             for (int o = 1; o < 32; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
             const float nm = fmaxf(mxh[k], cm);
@@ -1361,13 +1385,13 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_qh_kernel(const ReduceA
       const bool ok = k < C && warp_owns_tiles(w, T, nw, narrow);
       const int rec = ok ? static_cast<int>(seg0 + p0 + pi + w) : 0;
       wait_once();
-      const float lse = ok ? __ldg(a.rec_lse + static_cast<long long>(rec) * G + gg) : -INFINITY;
+      const float lse = ok ? ld_dep_f32(a.rec_lse + static_cast<long long>(rec) * G + gg) : -INFINITY;
       const int n = min(32, C - k0);
       float4 x[16];   // records of candidates 0..15, loaded before the weights are known
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int r = __shfl_sync(0xffffffffu, rec, i);
-        x[i] = i < n ? __ldg(rec_o + (static_cast<long long>(r) * G + gg) * (kD / 4) + lane)
+        x[i] = i < n ? ld_dep_f32x4(rec_o + (static_cast<long long>(r) * G + gg) * (kD / 4) + lane)
                      : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       float cm = lse;
@@ -1391,7 +1415,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_qh_kernel(const ReduceA
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int r = __shfl_sync(0xffffffffu, rec, 16 + i);
-          x[i] = 16 + i < n ? __ldg(rec_o + (static_cast<long long>(r) * G + gg) * (kD / 4) + lane)
+          x[i] = 16 + i < n ? ld_dep_f32x4(rec_o + (static_cast<long long>(r) * G + gg) * (kD / 4) + lane)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
@@ -1554,7 +1578,7 @@ cudaError_t launch_split_typed(DecodeArgs a, cudaStream_t s, int sms) {
   auto k = split_kernel<KMODE, GBIG, TQ>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, a.dyn_bytes);
   if (err != cudaSuccess) return err;
-  return launch_pdl(k, dim3(static_cast<unsigned>(sms)), dim3((sh.consumers + 1) * 32),
+  return launch_pdl(k, dim3(static_cast<unsigned>(sms)), dim3((sh.consumers + kProducers) * 32),
                     static_cast<size_t>(a.dyn_bytes), s, a);
 }
 

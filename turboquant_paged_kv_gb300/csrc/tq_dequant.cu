@@ -107,7 +107,7 @@ __device__ __forceinline__ void store8(void* base, long long elem, const float x
 }
 
 __device__ __forceinline__ float half_bits(const uint8_t* p) {
-  return __half2float(__ushort_as_half(__ldg(reinterpret_cast<const unsigned short*>(p))));
+  return __half2float(__ushort_as_half(ld_dep_u16(p)));
 }
 
 // One CTA per (sequence, 16-position tile, KV head): grid (seq_tiles * batch,
@@ -134,7 +134,7 @@ dequant_kernel(const DequantArgs a) {
   const bool in_out = p < a.max_seq_len;
   const long long elem = ((static_cast<long long>(b) * a.max_seq_len + p) * a.n_kv + h) * kD + 8 * l;
 
-  const int raw_len = __ldg(a.seq_lens + b);
+  const int raw_len = ld_dep_s32(a.seq_lens + b);
   if (p == 0 && h == 0 && lane == 0 && raw_len > a.len_cap && a.status) atomicOr(a.status, TQ_DEV_SEQ_TOO_LONG);
   const int len = min(max(raw_len, 0), a.len_cap);
   float k[8], v[8];
@@ -144,7 +144,7 @@ dequant_kernel(const DequantArgs a) {
   // holds a cached position
   int blk = -1;
   if (16 * t < len) {
-    blk = __ldg(a.block_table + static_cast<long long>(b) * a.bt_stride + ((16 * t) >> a.log2_bs));
+    blk = ld_dep_s32(a.block_table + static_cast<long long>(b) * a.bt_stride + ((16 * t) >> a.log2_bs));
     if ((blk < 0 || blk >= a.num_blocks) && threadIdx.x == 0 && a.status) atomicOr(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
   }
   const bool live = p < len && blk >= 0 && blk < a.num_blocks;
@@ -154,7 +154,7 @@ dequant_kernel(const DequantArgs a) {
                                         static_cast<long long>(a.tile_bytes);
     const uint8_t* krow = tile + a.k_off + r * a.k_row;
     if constexpr (KMODE == kFp8) {
-      const uint2 w = __ldg(reinterpret_cast<const uint2*>(krow + 8 * l));
+      const uint2 w = ld_dep_u32x2(krow + 8 * l);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t word = i < 2 ? w.x : w.y;
@@ -167,11 +167,10 @@ dequant_kernel(const DequantArgs a) {
     } else {
       uint32_t w;
       if constexpr (KMODE == kMse4) {
-        w = __ldg(reinterpret_cast<const uint32_t*>(krow + 4 * l));
+        w = ld_dep_u32(krow + 4 * l);
       } else {
         const uint8_t* g = krow + 3 * l;   // 24 bits, LSB first
-        w = static_cast<uint32_t>(__ldg(g)) | (static_cast<uint32_t>(__ldg(g + 1)) << 8) |
-            (static_cast<uint32_t>(__ldg(g + 2)) << 16);
+        w = ld_dep_u8(g) | (ld_dep_u8(g + 1) << 8) | (ld_dep_u8(g + 2) << 16);
       }
       const float nrm = half_bits(tile + a.knorm_off + 2 * r);
 #pragma unroll
@@ -182,8 +181,7 @@ dequant_kernel(const DequantArgs a) {
     // 16-byte groups swizzled by the pair index when rows are 64 bytes)
     const int pair = r >> 1;
     const int swz = (a.v_row % 64 == 0) ? 2 * (pair & 3) : 0;
-    const uint2 vw = __ldg(reinterpret_cast<const uint2*>(tile + a.v_off + pair * 2 * a.v_row +
-                                                          16 * ((l >> 1) ^ swz) + 8 * (l & 1)));
+    const uint2 vw = ld_dep_u32x2(tile + a.v_off + pair * 2 * a.v_row + 16 * ((l >> 1) ^ swz) + 8 * (l & 1));
     const uint32_t codes = ((vw.x >> (16 * (r & 1))) & 0xFFFFu) | (((vw.y >> (16 * (r & 1))) & 0xFFFFu) << 16);
     const float s = half_bits(tile + a.vscale_off + 2 * r);
     const float z = half_bits(tile + a.vzero_off + 2 * r);

@@ -60,7 +60,7 @@ enum KeyMode { kMse4 = 4, kMse3 = 3, kFp8 = 8 };
 
 template <typename T>
 __device__ __forceinline__ void load4(const void* base, long long elem, float out[4]) {
-  const uint2 raw = __ldg(reinterpret_cast<const uint2*>(static_cast<const T*>(base) + elem));
+  const uint2 raw = ld_dep_u32x2(static_cast<const T*>(base) + elem);
   if constexpr (std::is_same<T, __nv_bfloat16>::value) {
     const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
     const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
@@ -120,7 +120,7 @@ store_kernel(const StoreArgs a) {
                             ? static_cast<long long>(static_cast<unsigned>(vec) / static_cast<unsigned>(a.n_kv))
                             : vec / a.n_kv;
   const int head = static_cast<int>(vec - tok * a.n_kv);
-  const long long slot = a.slots[tok];
+  const long long slot = ld_dep_s64(a.slots + tok);
   if (slot < 0) return;
   const long long blk = slot >> a.log2_bs;
   const int off = static_cast<int>(slot & (a.block_size - 1));

@@ -28,6 +28,7 @@ rotated between steps, so no step finds its cache in L2.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
                   [--workload gqa|k3v4|k8v4|long|all] [--partition P]
   python bench.py --op dequant [--steps K] [--warmup W]   (full dequantisation alone)
+  python bench.py --op store [--workload W]               (the prefill-chunk store alone)
 
 ``--impl reference`` times the CPU oracle (test infrastructure) on a bounded
 sample of the same workload. N > 1 runs weak-scaling replicas, one process
@@ -687,6 +688,71 @@ def run_dequant(args):
     return 0
 
 
+def run_store(args):
+    """``--op store``: tq_store of the workload's prefill chunk (8192 bf16
+    tokens through random distinct slots; k8v4: its own chunk) into an empty
+    cache, one launch per step, timed alone with CUDA events. Prints one JSON
+    line of its own with the store kernel's roofline."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from turboquant_paged_kv_gb300 import build as tqbuild
+    tqbuild.build()
+    import turboquant_paged_kv_gb300 as tq
+    import workloads
+
+    name = DEFAULT_WORKLOAD if args.workload == "all" else args.workload
+    w = workloads.get(name)
+    cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size)
+    bits = key_bits(w.preset)
+    cb = tq.tq_build_codebook(w.d, bits) if bits else None
+    lay = tq.tq_layout_for(cfg)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    if w.store_tokens:
+        k, v, slots = workloads.make_inputs(w, device=dev).store_chunk(dev)
+        num_blocks = int(slots.max().item()) // w.block_size + 1
+    else:
+        num_blocks = 2 * STORE_TOKENS // w.block_size
+        k = torch.randn(STORE_TOKENS, w.n_kv, w.d, generator=g, device=dev).to(torch.bfloat16)
+        v = torch.randn(STORE_TOKENS, w.n_kv, w.d, generator=g, device=dev).to(torch.bfloat16)
+        slots = torch.randperm(num_blocks * w.block_size, generator=g, device=dev)[:STORE_TOKENS].to(torch.int64)
+    cache = torch.zeros(num_blocks * lay.block_bytes, dtype=torch.uint8, device=dev)
+    n = k.shape[0]
+    nbytes = n * (w.n_kv * (2 * w.d * 2 + lay.slot_bytes) + 8)
+    stream = torch.cuda.current_stream()
+
+    def step(_i=0):
+        tq.tq_store(cfg, cb, k, v, slots, cache)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else "0"
+    reps = max(args.steps, 200)
+    with ClockSampler(gpu_id) as clk:
+        ms = time_device(step, reps, stream)
+    peak, peak_src = _peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "op": "store", "metric": "store Mtok/s and GB/s (bf16 K/V read + packed slots written)",
+        "value": n / (ms * 1e-3) / 1e6, "unit": "Mtok/s", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "f32 arithmetic, bf16 in", "data": "synthetic",
+        "config": {"workload": _workload_text(w, f", {n}-token prefill chunk, random distinct slots"),
+                   "bytes_per_launch": nbytes},
+        "roofline": {"kernel": "store_kernel (tq_store)", "bound": "hbm", "achieved": gbs, "peak": peak,
+                     "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src, "ms_per_launch": ms,
+                     "issue_frac": _profile_field("tq_store.cu", f"store_{name}.md", "issue_active_frac"),
+                     "traffic": _profile_field("tq_store.cu", f"store_{name}.md", "dram_bytes_per_launch"),
+                     "algorithmic_bytes_per_launch": nbytes},
+        "gpu_launches": reps,
+        "clocks": clk.summary(),
+    }), flush=True)
+    return 0
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -698,8 +764,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dry-run", action="store_true",
                     help="run the multi-rank host logic on the CPU (gloo) without a GPU")
-    ap.add_argument("--op", default="decode", choices=["decode", "dequant"],
-                    help="decode: the decode step (default); dequant: tq_dequant of the gqa cache alone")
+    ap.add_argument("--op", default="decode", choices=["decode", "dequant", "store"],
+                    help="decode: the decode step (default); dequant: tq_dequant of the gqa cache alone; "
+                         "store: tq_store of the workload's prefill chunk alone")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -719,6 +786,8 @@ def main(argv=None):
         return run_dry(args)
     if args.op == "dequant":
         return run_dequant(args)
+    if args.op == "store":
+        return run_store(args)
     return run_reference(args) if args.impl == "reference" else run_tq(args)
 
 

@@ -77,6 +77,11 @@ __device__ __forceinline__ uint2 ld_dep_u32x2(const void* p) {
   asm volatile("ld.global.cg.v2.b32 {%0, %1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
+__device__ __forceinline__ uint4 ld_dep_u32x4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.b32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
 __device__ __forceinline__ float ld_dep_f32(const float* p) {
   float v;
   asm volatile("ld.global.cg.f32 %0, [%1];\n" : "=f"(v) : "l"(p));

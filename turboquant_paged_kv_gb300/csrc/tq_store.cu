@@ -1,5 +1,5 @@
 // tq_store: fused rotate / quantise / pack / write of K and V into the paged
-// cache, one warp per (token, KV head).
+// cache, one half-warp per (token, KV head).
 //
 // Method: "vLLM 源码完全拆解(十九):TurboQuant KV Cache 量化" (pinghaoyang.com.cn),
 // section "写入内核:store 路径如何旋转、量化与打包":
@@ -13,11 +13,15 @@
 //   slot < 0 writes nothing                                        ("融合 kernel 的骨架")
 //
 // Differences from the pages' design: the pages run the norm and the rotation
-// as a separate cuBLAS GEMM over a materialised fp32 copy of K; here the warp
-// holds the 128 coordinates in registers (4 per lane), rotates them with a
-// butterfly (2 in-lane stages + 5 xor-shuffle stages) and never writes an
-// intermediate. The value-quantisation arithmetic uses explicitly rounded fp32
-// operations (no contraction), so V codes are reproducible bit for bit.
+// as a separate cuBLAS GEMM over a materialised fp32 copy of K; here a
+// half-warp holds the 128 coordinates in registers (8 per lane: coordinate
+// 8 l + j in lane l of the half), rotates them with a butterfly (3 in-lane
+// stages + 4 xor-shuffle stages) and never writes an intermediate. Each warp
+// quantises two vectors at once, so every shuffle and reduction serves two
+// vectors and the per-lane work (bucketize, value codes) runs over 8
+// independent coordinates. The value-quantisation arithmetic uses explicitly
+// rounded fp32 operations (no contraction), so V codes are reproducible bit
+// for bit.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -34,6 +38,7 @@ namespace tq {
 namespace {
 
 constexpr int kStoreWarps = 8;
+constexpr int kVecsPerCta = 2 * kStoreWarps;   // a half-warp per vector
 constexpr int kD = 128;
 
 struct StoreArgs {
@@ -45,6 +50,7 @@ struct StoreArgs {
   long long num_vectors;     // num_tokens * n_kv
   long long num_blocks;
   int n_kv;
+  unsigned kv_magic, kv_shift;   // vec / n_kv = umulhi(2 vec, kv_magic) >> kv_shift (vec < 2^31)
   int block_size;
   int log2_bs;               // block_size is a power of two
   int tiles_per_block;
@@ -56,43 +62,61 @@ struct StoreArgs {
   float cent[16];
 };
 
+
 enum KeyMode { kMse4 = 4, kMse3 = 3, kFp8 = 8 };
 
+// 8 consecutive inputs (16 bytes) as floats.
 template <typename T>
-__device__ __forceinline__ void load4(const void* base, long long elem, float out[4]) {
-  const uint2 raw = ld_dep_u32x2(static_cast<const T*>(base) + elem);
-  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-    float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
-    out[0] = a.x; out[1] = a.y; out[2] = b.x; out[3] = b.y;
-  } else {
-    const __half2 lo = *reinterpret_cast<const __half2*>(&raw.x);
-    const __half2 hi = *reinterpret_cast<const __half2*>(&raw.y);
-    float2 a = __half22float2(lo), b = __half22float2(hi);
-    out[0] = a.x; out[1] = a.y; out[2] = b.x; out[3] = b.y;
+__device__ __forceinline__ void load8(const void* base, long long elem, float out[8]) {
+  const uint4 raw = ld_dep_u32x4(static_cast<const T*>(base) + elem);
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    else f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    out[2 * i] = f.x;
+    out[2 * i + 1] = f.y;
   }
 }
 
-__device__ __forceinline__ float warp_sum(float x) {
+// Sum, min and max over the 16 lanes of a half-warp (xor 1 .. 8 stay inside it).
+__device__ __forceinline__ float half_sum(float x) {
 #pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  for (int m = 1; m <= 8; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  return x;
+}
+__device__ __forceinline__ float half_min(float x) {
+#pragma unroll
+  for (int m = 1; m <= 8; m <<= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, m));
+  return x;
+}
+__device__ __forceinline__ float half_max(float x) {
+#pragma unroll
+  for (int m = 1; m <= 8; m <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, m));
   return x;
 }
 
-// Sylvester-order Walsh-Hadamard transform of the 128 coordinates held as
-// 4 consecutive values per lane (coordinate 4*lane + j).
-__device__ __forceinline__ void fwht128(float v[4], int lane) {
-  float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-  v[0] = a0 + a2; v[2] = a0 - a2; v[1] = a1 + a3; v[3] = a1 - a3;
+// Sylvester-order Walsh-Hadamard transform (unnormalised) of the 128
+// coordinates of a half-warp, coordinate 8 l + j in lane l: index bits 0-2 in
+// the lane, bits 3-6 across lanes l ^ 1 .. l ^ 8. The lane whose stride bit is
+// set keeps (partner - own), the other (own + partner).
+__device__ __forceinline__ void fwht128_half(float v[8], int l) {
 #pragma unroll
-  for (int m = 1; m <= 16; m <<= 1) {
-    const bool upper = lane & m;
+  for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float p = __shfl_xor_sync(0xffffffffu, v[j], m);
-      v[j] = upper ? (p - v[j]) : (v[j] + p);
+    for (int j = 0; j < 8; ++j) {
+      if (j & h) continue;
+      const float a = v[j], b = v[j + h];
+      v[j] = a + b;
+      v[j + h] = a - b;
     }
+  }
+#pragma unroll
+  for (int m = 1; m <= 8; m <<= 1) {
+    const float sgn = (l & m) ? -1.f : 1.f;   // one exact fma with +-1 per step
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = fmaf(sgn, v[j], __shfl_xor_sync(0xffffffffu, v[j], m));
   }
 }
 
@@ -100,7 +124,39 @@ __device__ __forceinline__ void flag(unsigned int* status, unsigned int bit) {
   if (status) atomicOr(status, bit);
 }
 
-template <int KMODE, typename T>
+// Codes of 8 values of one vector: trunc(fp32((v - min) / s) + 1/2), clamped
+// to [0, kLevels], with IEEE division as specified. The product with an
+// approximate reciprocal is within 4e-6 of the quotient (t <= 15), so
+// away from a rounding boundary it gives the same code; a value within 1e-5
+// of one takes the exact quotient, on a branch that is rarely taken (the
+// division is a long instruction sequence, so it must not run for every
+// coordinate).
+template <int kLevels>
+__device__ __forceinline__ void value_codes(const float v[8], float mn, float s, int q[8]) {
+  const float rs = __fdividef(1.f, s);   // approximate: within a few ulp, far inside the band
+  float dv[8];
+  uint32_t near = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    dv[j] = __fsub_rn(v[j], mn);
+    const float u = fmaf(dv[j], rs, 0.5f);
+    near |= fabsf(u - rintf(u)) < 1e-5f ? (1u << j) : 0u;
+    q[j] = __float2int_rz(u);
+  }
+  if (near) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if ((near >> j) & 1u) q[j] = __float2int_rz(__fadd_rn(__fdiv_rn(dv[j], s), 0.5f));
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) q[j] = min(q[j], kLevels);   // v >= min, so no code is negative
+}
+
+// Warp w of the CTA handles vectors 2 w and 2 w + 1 of the CTA's 16, one per
+// half-warp. A half whose vector is past the end, or whose slot is negative or
+// out of range, computes on zeros and writes nothing (its lanes stay for the
+// shuffles).
+template <int KMODE, int VBITS, typename T>
 __global__ void __launch_bounds__(kStoreWarps * 32)
 store_kernel(const StoreArgs a) {
   grid_dep_wait();   // inputs and cache may come from the previous kernel
@@ -113,47 +169,68 @@ store_kernel(const StoreArgs a) {
   __syncthreads();
 
   const int lane = threadIdx.x & 31;
-  const long long vec = static_cast<long long>(blockIdx.x) * kStoreWarps + (threadIdx.x >> 5);
-  if (vec >= a.num_vectors) return;
-  // vec / n_kv in 32 bits whenever the vector count allows
-  const long long tok = a.num_vectors < (1ll << 32)
-                            ? static_cast<long long>(static_cast<unsigned>(vec) / static_cast<unsigned>(a.n_kv))
-                            : vec / a.n_kv;
-  const int head = static_cast<int>(vec - tok * a.n_kv);
-  const long long slot = ld_dep_s64(a.slots + tok);
-  if (slot < 0) return;
-  const long long blk = slot >> a.log2_bs;
-  const int off = static_cast<int>(slot & (a.block_size - 1));
-  if (blk >= a.num_blocks) {
-    if (lane == 0) flag(a.status, TQ_DEV_SLOT_OUT_OF_RANGE);
-    return;
+  const int l = lane & 15;
+  const long long vec = static_cast<long long>(blockIdx.x) * kVecsPerCta + (threadIdx.x >> 4);
+  bool live = vec < a.num_vectors;
+  long long tok = 0;
+  int head = 0;
+  uint8_t* tile = nullptr;
+  int r = 0;
+  if (live) {
+    // vec / n_kv by multiply and shift whenever the vector count allows
+    tok = a.num_vectors < (1ll << 31)
+              ? static_cast<long long>(__umulhi(2u * static_cast<unsigned>(vec), a.kv_magic) >> a.kv_shift)
+              : vec / a.n_kv;
+    head = static_cast<int>(vec - tok * a.n_kv);
+    const long long slot = ld_dep_s64(a.slots + tok);
+    const long long blk = slot >> a.log2_bs;
+    if (slot < 0) {
+      live = false;
+    } else if (blk >= a.num_blocks) {
+      if (l == 0) flag(a.status, TQ_DEV_SLOT_OUT_OF_RANGE);
+      live = false;
+    } else {
+      const int off = static_cast<int>(slot & (a.block_size - 1));
+      tile = a.cache + ((blk * a.n_kv + head) * a.tiles_per_block + (off >> 4)) * static_cast<long long>(a.tile_bytes);
+      r = off & 15;
+    }
   }
-  uint8_t* tile = a.cache +
-      ((blk * a.n_kv + head) * a.tiles_per_block + (off >> 4)) * static_cast<long long>(a.tile_bytes);
-  const int r = off & 15;
 
-  float k[4], v[4];
-  load4<T>(a.key, vec * kD + lane * 4, k);
-  load4<T>(a.value, vec * kD + lane * 4, v);
+  float k[8], v[8];
+  if (live) {
+    load8<T>(a.key, vec * kD + 8 * l, k);
+    load8<T>(a.value, vec * kD + 8 * l, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) k[j] = v[j] = 0.f;
+  }
 
   // ---------------- keys ----------------
   if constexpr (KMODE == kFp8) {
-    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(k[0], k[1]), __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(k[2], k[3]), __NV_SATFINITE, __NV_E4M3);
-    const uint32_t w = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-    *reinterpret_cast<uint32_t*>(tile + a.k_off + r * a.k_row + 4 * lane) = w;
+    uint32_t w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(k[4 * i], k[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(k[4 * i + 2], k[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
+      w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    if (live) *reinterpret_cast<uint2*>(tile + a.k_off + r * a.k_row + 8 * l) = make_uint2(w[0], w[1]);
   } else {
-    float ss = k[0] * k[0];
-    ss = fmaf(k[1], k[1], ss);
-    ss = fmaf(k[2], k[2], ss);
-    ss = fmaf(k[3], k[3], ss);
-    const float n = __fsqrt_rn(warp_sum(ss));
-    fwht128(k, lane);
-    const float sc = __fdiv_rn(0.088388347648318440f, __fadd_rn(n, 1e-8f));   // 1/sqrt(128) / (n + 1e-8)
-    int idx[4];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss = fmaf(k[j], k[j], ss);
+    // The key's scalars use the hardware approximations (a few ulp): the
+    // pages' own pipeline forms y in fp32 through a matrix product, so y is
+    // only defined to fp32 rounding, and the index decisions are checked
+    // against the exact value with a 1e-5 band; the stored norm is an fp16.
+    const float ss16 = half_sum(ss);
+    const float n = ss16 > 0.f ? ss16 * rsqrtf(ss16) : 0.f;
+    fwht128_half(k, l);
+    const float sc = __fdividef(0.088388347648318440f, n + 1e-8f);   // 1/sqrt(128) / (n + 1e-8)
+    int idx[8];
     float cs = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
       const float y = k[j] * sc;
       // #{m : y >= mid_m} over the ascending midpoints, by binary search
       int c = 0;
@@ -163,71 +240,82 @@ store_kernel(const StoreArgs a) {
       const float cv = s_cent[c];
       cs = fmaf(cv, cv, cs);
     }
-    cs = warp_sum(cs);
-    const float stored = __fdiv_rn(n, __fsqrt_rn(__fadd_rn(cs, 1e-16f)));
-    if constexpr (KMODE == kMse4) {
-      const uint32_t w = idx[0] | (idx[1] << 4) | (idx[2] << 8) | (idx[3] << 12);
-      *reinterpret_cast<uint16_t*>(tile + a.k_off + r * a.k_row + 2 * lane) = static_cast<uint16_t>(w);
-    } else {
-      const uint32_t w12 = idx[0] | (idx[1] << 3) | (idx[2] << 6) | (idx[3] << 9);
-      const uint32_t partner = __shfl_xor_sync(0xffffffffu, w12, 1);
-      if ((lane & 1) == 0) {
-        const uint32_t w24 = w12 | (partner << 12);
-        uint8_t* dst = tile + a.k_off + r * a.k_row + 3 * (lane >> 1);
-        dst[0] = static_cast<uint8_t>(w24);
-        dst[1] = static_cast<uint8_t>(w24 >> 8);
-        dst[2] = static_cast<uint8_t>(w24 >> 16);
+    cs = half_sum(cs);
+    const float stored = n * rsqrtf(cs + 1e-16f);
+    uint32_t w = 0;   // LSB-first: coordinate 8 l + j at bit KMODE * j of the lane's run
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w |= static_cast<uint32_t>(idx[j]) << (KMODE * j);
+    if (live) {
+      uint8_t* row = tile + a.k_off + r * a.k_row;
+      if constexpr (KMODE == kMse4) {
+        *reinterpret_cast<uint32_t*>(row + 4 * l) = w;
+      } else {   // 3 bytes at 3 l
+        row[3 * l] = static_cast<uint8_t>(w);
+        row[3 * l + 1] = static_cast<uint8_t>(w >> 8);
+        row[3 * l + 2] = static_cast<uint8_t>(w >> 16);
       }
+      if (l == 0)
+        *reinterpret_cast<uint16_t*>(tile + a.knorm_off + 2 * r) = __half_as_ushort(__float2half_rn(stored));
     }
-    if (lane == 0)
-      *reinterpret_cast<uint16_t*>(tile + a.knorm_off + 2 * r) = __half_as_ushort(__float2half_rn(stored));
   }
 
-  // ---------------- values (4-bit) ----------------
-  float mn = fminf(fminf(v[0], v[1]), fminf(v[2], v[3]));
-  float mx = fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3]));
-  asm("redux.sync.min.f32 %0, %0, 0xffffffff;" : "+f"(mn));
-  asm("redux.sync.max.f32 %0, %0, 0xffffffff;" : "+f"(mx));
-  float s = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
-  s = (s > 1e-8f) ? s : 1e-8f;
-  // code = trunc(fp32((v - min) / s) + 1/2) with IEEE division, as specified.
-  // The product with the correctly rounded reciprocal is within 4e-6 of it
-  // (t <= 15), so away from a rounding boundary it gives the same code; within
-  // 1e-5 of one the exact quotient is taken.
-  const float rs = __frcp_rn(s);
-  uint32_t w = 0;
+  // ---------------- values ----------------
+  constexpr int kLevels = (1 << VBITS) - 1;
+  float mn = v[0], mx = v[0];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float dv = __fsub_rn(v[j], mn);
-    const float u = __fadd_rn(__fmul_rn(dv, rs), 0.5f);
-    const float fr = u - floorf(u);
-    int q = (fr < 1e-5f || fr > 1.f - 1e-5f) ? __float2int_rz(__fadd_rn(__fdiv_rn(dv, s), 0.5f)) : __float2int_rz(u);
-    q = min(max(q, 0), 15);
-    w |= static_cast<uint32_t>(q) << (4 * j);
+  for (int j = 1; j < 8; ++j) {
+    mn = fminf(mn, v[j]);
+    mx = fmaxf(mx, v[j]);
   }
-  // pair-interleaved 16-bit words, 16-byte groups swizzled by the pair index:
-  // word `lane` of token r = 2p + j
+  mn = half_min(mn);
+  mx = half_max(mx);
+  float s = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(kLevels));
+  s = (s > 1e-8f) ? s : 1e-8f;
+  int q[8];
+  value_codes<kLevels>(v, mn, s, q);
+  uint32_t w = 0;   // this lane's LSB-first run: coordinate 8 l + j at bit VBITS * j
+#pragma unroll
+  for (int j = 0; j < 8; ++j) w |= static_cast<uint32_t>(q[j]) << (VBITS * j);
+  // Pair-interleaved 16-bit words: word i of token r = 2 p + t sits at
+  // v_off + 2 p v_row + 16 ((i >> 2) ^ x) + 4 (i & 3) + 2 t, x = 2 (p & 3) when
+  // v_row is a multiple of 64, else 0.
   const int pair = r >> 1;
   const int swz = (a.v_row % 64 == 0) ? 2 * (pair & 3) : 0;
-  *reinterpret_cast<uint16_t*>(tile + a.v_off + pair * 2 * a.v_row + 16 * ((lane >> 2) ^ swz) + 4 * (lane & 3) +
-                               2 * (r & 1)) = static_cast<uint16_t>(w);
-  if (lane == 0) {
+  uint8_t* vbase = live ? tile + a.v_off + pair * 2 * a.v_row + 2 * (r & 1) : nullptr;
+  auto put_word = [&](int i, uint32_t bits16) {
+    *reinterpret_cast<uint16_t*>(vbase + 16 * ((i >> 2) ^ swz) + 4 * (i & 3)) = static_cast<uint16_t>(bits16);
+  };
+  if constexpr (VBITS == 4) {   // lane l holds words 2 l and 2 l + 1
+    if (live) {
+      put_word(2 * l, w);
+      put_word(2 * l + 1, w >> 16);
+    }
+  } else {   // 3-bit: lanes 2 m, 2 m + 1 hold the 48 bits of words 3 m .. 3 m + 2
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, w, 1);
+    if (live) {
+      const int m = l >> 1;
+      if ((l & 1) == 0) {
+        put_word(3 * m, w);                                      // bits 0-15
+        put_word(3 * m + 1, (w >> 16) | ((other & 0xFFu) << 8));  // bits 16-23 | partner's 0-7
+      } else {
+        put_word(3 * m + 2, w >> 8);                             // bits 8-23
+      }
+    }
+  }
+  if (live && l == 0) {
     *reinterpret_cast<uint16_t*>(tile + a.vscale_off + 2 * r) = __half_as_ushort(__float2half_rn(s));
     *reinterpret_cast<uint16_t*>(tile + a.vzero_off + 2 * r) = __half_as_ushort(__float2half_rn(mn));
   }
 }
 
-template <int KMODE>
+template <int KMODE, int VBITS>
 cudaError_t launch_store(const StoreArgs& a, int in_dtype, cudaStream_t stream) {
-  const long long blocks = (a.num_vectors + kStoreWarps - 1) / kStoreWarps;
-  cudaError_t err;
+  const long long blocks = (a.num_vectors + kVecsPerCta - 1) / kVecsPerCta;
   if (in_dtype == TQ_DTYPE_BF16)
-    err = launch_pdl(store_kernel<KMODE, __nv_bfloat16>, dim3(static_cast<unsigned>(blocks)), dim3(kStoreWarps * 32), 0,
-                     stream, a);
-  else
-    err = launch_pdl(store_kernel<KMODE, __half>, dim3(static_cast<unsigned>(blocks)), dim3(kStoreWarps * 32), 0,
-                     stream, a);
-  return err;
+    return launch_pdl(store_kernel<KMODE, VBITS, __nv_bfloat16>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(kStoreWarps * 32), 0, stream, a);
+  return launch_pdl(store_kernel<KMODE, VBITS, __half>, dim3(static_cast<unsigned>(blocks)), dim3(kStoreWarps * 32), 0,
+                    stream, a);
 }
 
 }  // namespace
@@ -254,7 +342,7 @@ extern "C" tq_status tq_store(const tq_config* cfg, const tq_codebook* cb,
     return TQ_ERR_MISALIGNED;
   if (dev_status && (reinterpret_cast<unsigned long long>(dev_status) & 3ull)) return TQ_ERR_MISALIGNED;
   const long long vectors = num_tokens * cfg->num_kv_heads;
-  if (vectors / kStoreWarps + 1 > 0x7fffffffll) return TQ_ERR_INVALID_ARG;
+  if (vectors / kVecsPerCta + 1 > 0x7fffffffll) return TQ_ERR_INVALID_ARG;
 
   StoreArgs a;
   a.key = key;
@@ -265,6 +353,16 @@ extern "C" tq_status tq_store(const tq_config* cfg, const tq_codebook* cb,
   a.num_vectors = vectors;
   a.num_blocks = num_blocks;
   a.n_kv = cfg->num_kv_heads;
+  // x / n = floor(x magic / 2^(31 + s)) = umulhi(2 x, magic) >> s for every
+  // x < 2^31, with s = ceil(log2 n) and magic = ceil(2^(31 + s) / n) < 2^32:
+  // the excess magic n - 2^(31 + s) is below n, so x times it stays below
+  // 2^(31 + s) and never carries the quotient past the next integer
+  {
+    unsigned sh = 0;
+    while ((1u << sh) < static_cast<unsigned>(a.n_kv)) ++sh;
+    a.kv_shift = sh;
+    a.kv_magic = static_cast<unsigned>(((1ull << (31 + sh)) + a.n_kv - 1) / a.n_kv);
+  }
   a.block_size = cfg->block_size;
   a.log2_bs = __builtin_ctz(static_cast<unsigned>(cfg->block_size));
   a.tiles_per_block = cfg->block_size / kTileTokens;
@@ -281,8 +379,9 @@ extern "C" tq_status tq_store(const tq_config* cfg, const tq_codebook* cb,
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err;
-  if (L.key_fp8) err = launch_store<kFp8>(a, in_dtype, s);
-  else if (L.key_bits == 4) err = launch_store<kMse4>(a, in_dtype, s);
-  else err = launch_store<kMse3>(a, in_dtype, s);
+  if (L.key_fp8) err = launch_store<kFp8, 4>(a, in_dtype, s);
+  else if (L.key_bits == 4) err = launch_store<kMse4, 4>(a, in_dtype, s);
+  else if (L.value_bits == 4) err = launch_store<kMse3, 4>(a, in_dtype, s);
+  else err = launch_store<kMse3, 3>(a, in_dtype, s);
   return err == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

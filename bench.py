@@ -14,6 +14,7 @@ quoted on):
   k8v4  batch 128 x 8192, n_q 32, n_kv 8, k8v4 (e4m3 keys); its store line
         is the workload's own 8192-token prefill chunk
   long  batch 4 x 131072, n_q 64, n_kv 8, 4bit_nc, Student-t outlier channels
+  3bit  the gqa shape with the 3bit_nc preset (3-bit keys and 3-bit values)
   all   every workload above, one JSON line each
 
 ``value`` = logical packed-KV bytes read per step / step time (GB/s). Each
@@ -56,7 +57,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode KV-read GB/s & % of HBM peak; decode tok/s; store Mtok/s (d=128 4bit_nc)"
-WORKLOADS = ("gqa", "k3v4", "k8v4", "long")
+WORKLOADS = ("gqa", "k3v4", "k8v4", "long", "3bit")
 DEFAULT_WORKLOAD = "gqa"
 # tokens of one sequence the CPU oracle handles per step in the baseline legs
 ORACLE_SAMPLE_TOKENS = 8192
@@ -554,6 +555,7 @@ def run_workload(tq, name: str, args, dev, world: int, rank: int):
         "vs_baseline": None,
         "dtype": "f16 mma / f32 accumulate over %s codes" % ("e4m3 key" if w.preset == "k8v4" else
                                                              "%d-bit key" % key_bits(w.preset)),
+        "value_bits": c.lay.value_bits,
         "data": "synthetic",
         "config": {"workload": _workload_text(w, ", bf16 in/out"),
                    "partition_tokens": args.partition, "split": split_note,

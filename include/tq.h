@@ -301,7 +301,7 @@ const char* tq_status_string(int status);
 /* Host. ABI version of this header (major * 100 + minor). */
 int tq_version(void);
 
-#define TQ_ABI_VERSION 101   /* 1.01: tq_dequant added */
+#define TQ_ABI_VERSION 102   /* 1.01: tq_dequant added; 1.02: 3bit_nc (3-bit values) runs */
 
 #ifdef __cplusplus
 }

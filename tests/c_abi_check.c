@@ -49,7 +49,9 @@ int main(void) {
   if (tq_dequant(&cfg, &cb, NULL, 1, NULL, 1, NULL, 0, 16, NULL, NULL, TQ_DTYPE_BF16, NULL, NULL) != TQ_OK)
     return fail("dequant empty batch");
   cfg.preset = TQ_PRESET_3BIT_NC;
-  if (tq_layout_for(&cfg, &lay) != TQ_ERR_UNSUPPORTED) return fail("3bit_nc unsupported");
+  if (tq_layout_for(&cfg, &lay) != TQ_OK || lay.slot_bytes != 102 || lay.v_row_bytes != 48) return fail("3bit_nc layout");
+  cfg.head_dim = 96;
+  if (tq_layout_for(&cfg, &lay) != TQ_ERR_UNSUPPORTED) return fail("d 96 unsupported");
   if (strlen(tq_status_string(TQ_ERR_UNSUPPORTED)) == 0) return fail("status string");
   printf("errors ok: %s\n", tq_status_string(TQ_ERR_UNSUPPORTED));
   printf("ALL OK\n");

@@ -36,6 +36,11 @@ from oracle import layout as olay
 from oracle import numerics
 from oracle import store as ost
 
+def key_bits(preset: str):
+    """Codebook bits of a preset's keys (None for e4m3 keys)."""
+    return {"4bit_nc": 4, "k3v4_nc": 3, "3bit_nc": 3}.get(preset)
+
+
 BOUNDARY_BAND = 1e-5
 MAX_MISMATCH_FRACTION = 1e-4
 DECODE_ATOL = 2e-3

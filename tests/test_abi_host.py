@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(tq):
     assert sorted(_abi.EXPORTED) == declared
     # matches the header's TQ_ABI_VERSION
     text = open(os.path.join(ROOT, "include", "tq.h")).read()
-    assert tq.tq_version() == int(re.search(r"#define TQ_ABI_VERSION (\d+)", text).group(1)) == 101
+    assert tq.tq_version() == int(re.search(r"#define TQ_ABI_VERSION (\d+)", text).group(1)) == 102
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
@@ -57,7 +57,7 @@ def test_host_codebook_equals_oracle(tq, d, bits):
     assert np.array_equal(np.array(cb.midpoints[: n - 1], dtype=np.float32), ocb.midpoints_fp32(ref))
 
 
-@pytest.mark.parametrize("preset", ["k8v4", "4bit_nc", "k3v4_nc"])
+@pytest.mark.parametrize("preset", ["k8v4", "4bit_nc", "k3v4_nc", "3bit_nc"])
 @pytest.mark.parametrize("bs", [16, 32, 64, 128])
 def test_layout_equals_oracle(tq, preset, bs):
     cfg = tq.make_config(preset, 32, 8, block_size=bs)
@@ -77,7 +77,7 @@ def test_unsupported_shapes(tq):
     for cfg, want in [(tq.make_config("4bit_nc", 8, 8, head_dim=96), _abi.TQ_ERR_UNSUPPORTED),
                       (tq.make_config("4bit_nc", 8, 8, block_size=8), _abi.TQ_ERR_UNSUPPORTED),
                       (tq.make_config(17, 8, 8), _abi.TQ_ERR_INVALID_ARG),
-                      (tq.make_config("3bit_nc", 8, 8), _abi.TQ_ERR_UNSUPPORTED),
+                      (tq.make_config("3bit_nc", 8, 8), _abi.TQ_OK),
                       (tq.make_config("4bit_nc", 8, 8, flags=2), _abi.TQ_ERR_INVALID_ARG),
                       (tq.make_config("4bit_nc", 8, 8, flags=tq.TQ_FLAG_INDICES_READY), _abi.TQ_OK)]:
         assert lib.tq_layout_for(ctypes.byref(cfg), ctypes.byref(lay)) == want
@@ -158,7 +158,7 @@ def test_dequant_argument_errors_return_before_launch(tq):
     assert dq(dtype=7) == _abi.TQ_ERR_INVALID_ARG
     assert dq(stride=0) == _abi.TQ_ERR_INVALID_ARG
     assert dq(batch=-1) == _abi.TQ_ERR_INVALID_ARG
-    assert dq(cfg_=tq.make_config("3bit_nc", 32, 8), cb_=cb3) == _abi.TQ_ERR_UNSUPPORTED
+    assert dq(cfg_=tq.make_config("3bit_nc", 32, 8, head_dim=64), cb_=cb3) == _abi.TQ_ERR_UNSUPPORTED
     assert dq(cfg_=tq.make_config("4bit_nc", 32, 8, block_size=24)) == _abi.TQ_ERR_UNSUPPORTED
     # FP8 keys need no codebook; this call would launch, so only the argument
     # checks that come first are exercised

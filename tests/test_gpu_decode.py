@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import workloads
-from parity import OracleCache, assert_decode_close, cosine, unquantized_attention
+from parity import OracleCache, assert_decode_close, cosine, key_bits, unquantized_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +43,7 @@ def gpu_decode(tq, w, inp, cache_np, out_dtype=torch.float32, partition_tokens=N
     cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size,
                          partition_tokens=w.partition_tokens if partition_tokens is None else partition_tokens,
                          flags=flags)
-    cb = None if w.preset == "k8v4" else tq.tq_build_codebook(w.d, 3 if w.preset.startswith("k3") else 4)
+    cb = None if w.preset == "k8v4" else tq.tq_build_codebook(w.d, key_bits(w.preset))
     cache = torch.from_numpy(cache_np).cuda()
     lens = (inp.seq_lens if seq_lens is None else seq_lens).cuda()
     table = (inp.block_table if block_table is None else block_table).cuda()
@@ -59,7 +59,7 @@ def gpu_decode(tq, w, inp, cache_np, out_dtype=torch.float32, partition_tokens=N
 # partition_tokens None: the workload's own (fixed partitions, split + reduce
 # kernels); 0: stream-K, where tq_decode merges in the split kernel itself
 @pytest.mark.parametrize("pt", [None, 0])
-@pytest.mark.parametrize("name", ["tiny", "gqa_small", "k3v4_small", "k8v4_small", "long_small"])
+@pytest.mark.parametrize("name", ["tiny", "gqa_small", "k3v4_small", "k8v4_small", "long_small", "3bit_small"])
 def test_decode_matches_oracle_f32(tq, name, pt):
     w, inp, oc, q, ref = oracle_case(name)
     got = gpu_decode(tq, w, inp, oc.cache, partition_tokens=pt)
@@ -71,7 +71,7 @@ def test_decode_matches_oracle_f32(tq, name, pt):
 
 
 @pytest.mark.parametrize("pt", [None, 0])
-@pytest.mark.parametrize("name", ["tiny", "gqa_small", "long_small"])
+@pytest.mark.parametrize("name", ["tiny", "gqa_small", "long_small", "3bit_small"])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 def test_decode_matches_oracle_16bit_out(tq, name, dtype, pt):
     w, inp, oc, q, ref = oracle_case(name)

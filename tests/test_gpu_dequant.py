@@ -15,7 +15,7 @@ import torch
 import workloads
 from oracle import decode as od
 from oracle import dequant as dq
-from parity import OracleCache, assert_decode_close, assert_dequant_close
+from parity import OracleCache, assert_decode_close, assert_dequant_close, key_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +43,7 @@ def oracle_case(name, **over):
 
 def _config(tq, w):
     cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size)
-    cb = None if w.preset == "k8v4" else tq.tq_build_codebook(w.d, 3 if w.preset.startswith("k3") else 4)
+    cb = None if w.preset == "k8v4" else tq.tq_build_codebook(w.d, key_bits(w.preset))
     return cfg, cb
 
 
@@ -67,7 +67,7 @@ def oracle_dequant(oc, seq_lens, block_table, max_seq_len):
                          max_seq_len)
 
 
-@pytest.mark.parametrize("name", ["tiny", "gqa_small", "k3v4_small", "k8v4_small", "long_small"])
+@pytest.mark.parametrize("name", ["tiny", "gqa_small", "k3v4_small", "k8v4_small", "long_small", "3bit_small"])
 def test_dequant_matches_oracle_f32(tq, name):
     w, inp, oc = oracle_case(name)
     gk, gv = gpu_dequant(tq, w, inp, oc.cache)
@@ -76,7 +76,7 @@ def test_dequant_matches_oracle_f32(tq, name):
     print(f"{name}: max key error {ek:.2e}, max value error {ev:.2e}")
 
 
-@pytest.mark.parametrize("name", ["tiny", "gqa_small", "k8v4_small"])
+@pytest.mark.parametrize("name", ["tiny", "gqa_small", "k8v4_small", "3bit_small"])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 def test_dequant_matches_oracle_16bit_out(tq, name, dtype):
     w, inp, oc = oracle_case(name)

@@ -25,7 +25,7 @@ from oracle import codebook as ocb
 from oracle import decode as od
 from oracle import layout as olay
 from oracle import store as ost
-from parity import assert_decode_close, compare_store
+from parity import assert_decode_close, compare_store, key_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -36,6 +36,7 @@ CASES = {
     # (ragged last partition; 256 partitions per sequence for long)
     "gqa": ((0, 17, 31), (0, 13, 31), 0),
     "k3v4": ((0, 40, 63), (3, 30), 512),
+    "3bit": ((0, 31), (2, 29), 0),
     "k8v4": ((5, 127), (0, 21), 0),
     "long": ((1,), (0, 37), 512),
 }
@@ -85,7 +86,7 @@ def test_fullsize_sampled_parity(tq, name):
     host = workloads.make_inputs(w, "cpu")          # tables, lengths, queries
     spec = _OracleSpec(w)
     cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size, partition_tokens=part)
-    bits = {"4bit_nc": 4, "k3v4_nc": 3}.get(w.preset)
+    bits = key_bits(w.preset)
     cb = tq.tq_build_codebook(w.d, bits) if bits else None
     lay = tq.tq_layout_for(cfg)
     bb = lay.block_bytes

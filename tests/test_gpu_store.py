@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import workloads
-from parity import OracleCache, compare_store
+from parity import OracleCache, compare_store, key_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -23,7 +23,7 @@ def tq():
 def _gpu_fill(tq, w, inp, kv_cpu, status=None):
     lay = tq.tq_layout_for(tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size))
     cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size)
-    cb = None if w.preset == "k8v4" else tq.tq_build_codebook(w.d, 3 if w.preset.startswith("k3") else 4)
+    cb = None if w.preset == "k8v4" else tq.tq_build_codebook(w.d, key_bits(w.preset))
     cache = torch.full((inp.num_blocks * lay.block_bytes,), 0xA5, dtype=torch.uint8, device="cuda")
     k = torch.cat([kv[0] for kv in kv_cpu]).cuda()
     v = torch.cat([kv[1] for kv in kv_cpu]).cuda()
@@ -35,7 +35,7 @@ def _gpu_fill(tq, w, inp, kv_cpu, status=None):
 
 @pytest.mark.parametrize("name,bs", [("tiny", 16), ("gqa_small", 16), ("gqa_small", 32), ("gqa_small", 64),
                                      ("gqa_small", 128), ("k3v4_small", 16), ("k8v4_small", 16),
-                                     ("long_small", 16)])
+                                     ("long_small", 16), ("3bit_small", 16), ("3bit_small", 64)])
 def test_store_matches_oracle(tq, name, bs):
     w = workloads.get(name, block_size=bs)
     inp = workloads.make_inputs(w)

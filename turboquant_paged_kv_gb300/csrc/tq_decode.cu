@@ -329,6 +329,30 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
+// w >> n for n >= 0, w << -n otherwise (n is a compile-time constant here).
+__device__ __forceinline__ uint32_t shift_right(uint32_t w, int n) { return n >= 0 ? w >> n : w << -n; }
+
+// Value codes as mma A operands. The cache interleaves the 16-bit words of a
+// token pair, so a 32-bit word holds the same 16-bit word of both tokens, and
+// one mask turns code t of this lane into a half2 of the two tokens' codes as
+// exact fp16 subnormals at bit p (value code * 2^(p - 24)). x[] holds the
+// lane's words of one pair:
+//   4-bit: x[k] = word 4 g + k (coordinates 16 g + 4 k .. + 3), code t at bit 4 t;
+//   3-bit: x[k] = word 3 g + k (48 bits from bit 48 g), code t at bit 3 t, where
+//          codes 5 and 10 straddle two words and take one bit field from each.
+template <int VBITS>
+__device__ __forceinline__ uint32_t code_field(const uint4& x, int t, int p) {
+  if constexpr (VBITS == 4) {
+    return shift_right(word_of(x, t >> 2), 4 * (t & 3) - p) & (0x000F000Fu << p);
+  } else {
+    const int bit = 3 * t, wi = bit >> 4, s = bit & 15;
+    if (s <= 13) return shift_right(word_of(x, wi), s - p) & (0x00070007u << p);
+    const int nlo = 16 - s, nhi = 3 - nlo;   // bits from word wi, from word wi + 1
+    return (shift_right(word_of(x, wi), s - p) & ((((1u << nlo) - 1) << p) * 0x10001u)) |
+           (shift_right(word_of(x, wi + 1), -(nlo + p)) & ((((1u << nhi) - 1) << (p + nlo)) * 0x10001u));
+  }
+}
+
 // ---------------------------------------------------------------- LUT
 
 // Entry e (a key byte, or a 6-bit pair of 3-bit indices) holds 32 copies of
@@ -664,7 +688,7 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
 //     2 (c & 1), 2 (c & 1) + 1 and one exchange gives both the full score.
 //   G > 4: column k is head k; the lo parts run in a second mma into the same
 //     accumulators.
-template <int KMODE, int GBIG, typename TQ>
+template <int KMODE, int GBIG, int VBITS, typename TQ>
 __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, uint32_t qslots, uint32_t first,
                               uint32_t lut,
                               uint32_t klut) {
@@ -862,12 +886,18 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
 
     // ---- value words of the tiles, read now so the stage can be released
     // before the softmax and O^T: the producer refills it half a chunk earlier
-    uint4 vwa[NT], vwb[NT];   // tokens 2c, 2c+1 and 2c+8, 2c+9 of this lane's 16-byte groups
+    uint4 vwa[NT], vwb[NT];   // the lane's words of token pairs (2c, 2c+1) and (2c+8, 2c+9)
 #pragma unroll
     for (int i = 0; i < NT; ++i) {
-      const uint32_t vt = st + i * a.tile_bytes + a.v_off + 16 * (g ^ (2 * c));
-      vwa[i] = lds128(vt + 128 * c);
-      vwb[i] = lds128(vt + 128 * (c + 4));
+      if constexpr (VBITS == 4) {   // 16-byte group g of each pair, swizzled by 2 c
+        const uint32_t vt = st + i * a.tile_bytes + a.v_off + 16 * (g ^ (2 * c));
+        vwa[i] = lds128(vt + 128 * c);
+        vwb[i] = lds128(vt + 128 * (c + 4));
+      } else {                      // 12 bytes at 12 g of each 96-byte pair
+        const uint32_t vt = st + i * a.tile_bytes + a.v_off + 12 * g;
+        vwa[i] = make_uint4(lds32(vt + 96 * c), lds32(vt + 96 * c + 4), lds32(vt + 96 * c + 8), 0u);
+        vwb[i] = make_uint4(lds32(vt + 96 * (c + 4)), lds32(vt + 96 * (c + 4) + 4), lds32(vt + 96 * (c + 4) + 8), 0u);
+      }
     }
     auto release = [&]() {   // every lane has read the stage (values, norms, scales, zeros)
       if (release_bar) {
@@ -940,13 +970,9 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
         const uint32_t b0 = movmatrix_trans(lo_lane ? recv : hi), b1 = movmatrix_trans(lo_lane ? lo : recv);
         const uint4 va = vwa[i], vb = vwb[i];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t wa = word_of(va, k), wb = word_of(vb, k);
-          const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-          mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0, b1);
-          mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0,
-                   b1);
-        }
+        for (int mt = 0; mt < 8; ++mt)   // rows g, g + 8 of tile mt: coordinates 16 g + 2 mt, + 1
+          mma16816(o[mt], code_field<VBITS>(va, 2 * mt, 0), code_field<VBITS>(va, 2 * mt + 1, 4),
+                   code_field<VBITS>(vb, 2 * mt, 0), code_field<VBITS>(vb, 2 * mt + 1, 4), b0, b1);
       }
       return;
     }
@@ -1015,16 +1041,11 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
       if (GBIG) { b0l = movmatrix_trans(lg); b1l = movmatrix_trans(lh); }
       const uint4 va = vwa[i], vb = vwb[i];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t wa = word_of(va, k), wb = word_of(vb, k);
-        const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-        mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0, b1);
-        mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0, b1);
-        if (GBIG) {
-          mma16816(o[2 * k], wa & 0x000F000Fu, wa & 0x00F000F0u, wb & 0x000F000Fu, wb & 0x00F000F0u, b0l, b1l);
-          mma16816(o[2 * k + 1], wa8 & 0x000F000Fu, wa8 & 0x00F000F0u, wb8 & 0x000F000Fu, wb8 & 0x00F000F0u, b0l,
-                   b1l);
-        }
+      for (int mt = 0; mt < 8; ++mt) {   // rows g, g + 8 of tile mt: coordinates 16 g + 2 mt, + 1
+        const uint32_t a0 = code_field<VBITS>(va, 2 * mt, 0), a1 = code_field<VBITS>(va, 2 * mt + 1, 4);
+        const uint32_t a2 = code_field<VBITS>(vb, 2 * mt, 0), a3 = code_field<VBITS>(vb, 2 * mt + 1, 4);
+        mma16816(o[mt], a0, a1, a2, a3, b0, b1);
+        if (GBIG) mma16816(o[mt], a0, a1, a2, a3, b0l, b1l);
       }
     }
   };
@@ -1084,7 +1105,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
 
 // Warps 0 .. kProducers - 1 are producers; the rest are the W consumers. One
 // CTA per SM.
-template <int KMODE, int GBIG, typename TQ>
+template <int KMODE, int GBIG, int VBITS, typename TQ>
 __global__ void __launch_bounds__((kMaxConsumers + kProducers) * 32, 1)
 split_kernel(const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t s_dyn[];
@@ -1125,7 +1146,7 @@ split_kernel(const DecodeArgs a) {
     asm volatile("bar.sync 1, %0;\n" ::"r"(blockDim.x) : "memory");
     grid_dep_wait();   // already resolved: the producers passed it before arriving
     grid_dep_launch();
-    consumer_warp<KMODE, GBIG, TQ>(a, W, warp - kProducers, bars, qslots, first, lut, kLut);
+    consumer_warp<KMODE, GBIG, VBITS, TQ>(a, W, warp - kProducers, bars, qslots, first, lut, kLut);
   }
 }
 
@@ -1567,7 +1588,7 @@ bool launch_shape(int tile_bytes, int group, LaunchShape* s) {
   return true;
 }
 
-template <int KMODE, int GBIG, typename TQ>
+template <int KMODE, int GBIG, int VBITS, typename TQ>
 cudaError_t launch_split_typed(DecodeArgs a, cudaStream_t s, int sms) {
   LaunchShape sh;
   if (!launch_shape<KMODE>(a.tile_bytes, a.group, &sh)) return cudaErrorInvalidConfiguration;
@@ -1575,20 +1596,20 @@ cudaError_t launch_split_typed(DecodeArgs a, cudaStream_t s, int sms) {
   a.desc_off = sh.desc_off;
   a.dyn_bytes = sh.dyn_bytes;
   a.qbuf_bytes = a.group * kD * 2;
-  auto k = split_kernel<KMODE, GBIG, TQ>;
+  auto k = split_kernel<KMODE, GBIG, VBITS, TQ>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, a.dyn_bytes);
   if (err != cudaSuccess) return err;
   return launch_pdl(k, dim3(static_cast<unsigned>(sms)), dim3((sh.consumers + kProducers) * 32),
                     static_cast<size_t>(a.dyn_bytes), s, a);
 }
 
-template <int KMODE>
+template <int KMODE, int VBITS>
 cudaError_t launch_split(const DecodeArgs& a, int q_dtype, cudaStream_t s, int sms) {
   if (q_dtype == TQ_DTYPE_BF16)
-    return a.group > 4 ? launch_split_typed<KMODE, 1, __nv_bfloat16>(a, s, sms)
-                       : launch_split_typed<KMODE, 0, __nv_bfloat16>(a, s, sms);
-  return a.group > 4 ? launch_split_typed<KMODE, 1, __half>(a, s, sms)
-                     : launch_split_typed<KMODE, 0, __half>(a, s, sms);
+    return a.group > 4 ? launch_split_typed<KMODE, 1, VBITS, __nv_bfloat16>(a, s, sms)
+                       : launch_split_typed<KMODE, 0, VBITS, __nv_bfloat16>(a, s, sms);
+  return a.group > 4 ? launch_split_typed<KMODE, 1, VBITS, __half>(a, s, sms)
+                     : launch_split_typed<KMODE, 0, VBITS, __half>(a, s, sms);
 }
 
 // Consumer warps per CTA of the split launch (the reduce needs the count).
@@ -1665,9 +1686,10 @@ tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* 
     a.cent[i] = (!P.L.key_fp8 && i < cb->num_levels) ? static_cast<float>(static_cast<double>(gamma) * cb->centroids[i]) : 0.f;
 
   cudaError_t err;
-  if (P.L.key_fp8) err = launch_split<kFp8>(a, q_dtype, stream, P.sms);
-  else if (P.L.key_bits == 4) err = launch_split<kMse4>(a, q_dtype, stream, P.sms);
-  else err = launch_split<kMse3>(a, q_dtype, stream, P.sms);
+  if (P.L.key_fp8) err = launch_split<kFp8, 4>(a, q_dtype, stream, P.sms);
+  else if (P.L.key_bits == 4) err = launch_split<kMse4, 4>(a, q_dtype, stream, P.sms);
+  else if (P.L.value_bits == 4) err = launch_split<kMse3, 4>(a, q_dtype, stream, P.sms);
+  else err = launch_split<kMse3, 3>(a, q_dtype, stream, P.sms);
   return err == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
 

@@ -113,7 +113,7 @@ __device__ __forceinline__ float half_bits(const uint8_t* p) {
 // One CTA per (sequence, 16-position tile, KV head): grid (seq_tiles * batch,
 // n_kv). Warp w expands positions 2w and 2w + 1 of the tile, one per
 // half-warp; lane l of a half holds coordinates 8l .. 8l + 7.
-template <int KMODE, typename T>
+template <int KMODE, int VBITS, typename T>
 __global__ void __launch_bounds__(kDequantWarps * 32)
 dequant_kernel(const DequantArgs a) {
   grid_dep_wait();   // cache, tables and lengths may come from the previous kernel
@@ -176,17 +176,30 @@ dequant_kernel(const DequantArgs a) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) k[j] = nrm * s_cent[(w >> (KMODE * j)) & ((1u << KMODE) - 1)];
     }
-    // value words 2l and 2l + 1 of token r = 2 * pair + (r & 1): one 8-byte
-    // group holding both words of both tokens of the pair (pair-interleaved,
-    // 16-byte groups swizzled by the pair index when rows are 64 bytes)
     const int pair = r >> 1;
-    const int swz = (a.v_row % 64 == 0) ? 2 * (pair & 3) : 0;
-    const uint2 vw = ld_dep_u32x2(tile + a.v_off + pair * 2 * a.v_row + 16 * ((l >> 1) ^ swz) + 8 * (l & 1));
-    const uint32_t codes = ((vw.x >> (16 * (r & 1))) & 0xFFFFu) | (((vw.y >> (16 * (r & 1))) & 0xFFFFu) << 16);
+    uint32_t codes;   // this lane's codes, LSB-first: coordinate 8 l + j at bit VBITS j
+    if constexpr (VBITS == 4) {
+      // value words 2l and 2l + 1 of token r = 2 * pair + (r & 1): one 8-byte
+      // group holding both words of both tokens of the pair (pair-interleaved,
+      // 16-byte groups swizzled by the pair index when rows are 64 bytes)
+      const int swz = (a.v_row % 64 == 0) ? 2 * (pair & 3) : 0;
+      const uint2 vw = ld_dep_u32x2(tile + a.v_off + pair * 2 * a.v_row + 16 * ((l >> 1) ^ swz) + 8 * (l & 1));
+      codes = ((vw.x >> (16 * (r & 1))) & 0xFFFFu) | (((vw.y >> (16 * (r & 1))) & 0xFFFFu) << 16);
+    } else {
+      // 24 bits from bit 24 l of the token's stream: 16-bit words 3 m and
+      // 3 m + 1 (l = 2 m, bits 0-23 of the pair) or 3 m + 1 and 3 m + 2 (l =
+      // 2 m + 1, bits 8-31); the pair's 32-bit word i (no swizzle at 48-byte
+      // rows) holds word i of both tokens
+      const int w0 = 3 * (l >> 1) + (l & 1);
+      const uint8_t* pw = tile + a.v_off + pair * 2 * a.v_row + 4 * w0;
+      const int sh = 16 * (r & 1);
+      const uint32_t lo = (ld_dep_u32(pw) >> sh) & 0xFFFFu, hi = (ld_dep_u32(pw + 4) >> sh) & 0xFFFFu;
+      codes = (lo | (hi << 16)) >> (8 * (l & 1));
+    }
     const float s = half_bits(tile + a.vscale_off + 2 * r);
     const float z = half_bits(tile + a.vzero_off + 2 * r);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = fmaf(s, static_cast<float>((codes >> (4 * j)) & 15u), z);
+    for (int j = 0; j < 8; ++j) v[j] = fmaf(s, static_cast<float>((codes >> (VBITS * j)) & ((1u << VBITS) - 1)), z);
   }
   if constexpr (KMODE != kFp8) {
     // every half-warp of the warp runs the butterfly (its shuffles need all
@@ -201,13 +214,14 @@ dequant_kernel(const DequantArgs a) {
   }
 }
 
-template <int KMODE>
+template <int KMODE, int VBITS>
 cudaError_t launch_dequant(const DequantArgs& a, int batch, int out_dtype, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(static_cast<long long>(a.seq_tiles) * batch), static_cast<unsigned>(a.n_kv));
   const dim3 block(kDequantWarps * 32);
-  if (out_dtype == TQ_DTYPE_BF16) return launch_pdl(dequant_kernel<KMODE, __nv_bfloat16>, grid, block, 0, stream, a);
-  if (out_dtype == TQ_DTYPE_F16) return launch_pdl(dequant_kernel<KMODE, __half>, grid, block, 0, stream, a);
-  return launch_pdl(dequant_kernel<KMODE, float>, grid, block, 0, stream, a);
+  if (out_dtype == TQ_DTYPE_BF16)
+    return launch_pdl(dequant_kernel<KMODE, VBITS, __nv_bfloat16>, grid, block, 0, stream, a);
+  if (out_dtype == TQ_DTYPE_F16) return launch_pdl(dequant_kernel<KMODE, VBITS, __half>, grid, block, 0, stream, a);
+  return launch_pdl(dequant_kernel<KMODE, VBITS, float>, grid, block, 0, stream, a);
 }
 
 }  // namespace
@@ -265,8 +279,9 @@ extern "C" tq_status tq_dequant(const tq_config* cfg, const tq_codebook* cb,
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err;
-  if (L.key_fp8) err = launch_dequant<kFp8>(a, batch, out_dtype, s);
-  else if (L.key_bits == 4) err = launch_dequant<kMse4>(a, batch, out_dtype, s);
-  else err = launch_dequant<kMse3>(a, batch, out_dtype, s);
+  if (L.key_fp8) err = launch_dequant<kFp8, 4>(a, batch, out_dtype, s);
+  else if (L.key_bits == 4) err = launch_dequant<kMse4, 4>(a, batch, out_dtype, s);
+  else if (L.value_bits == 4) err = launch_dequant<kMse3, 4>(a, batch, out_dtype, s);
+  else err = launch_dequant<kMse3, 3>(a, batch, out_dtype, s);
   return err == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

@@ -31,7 +31,6 @@ tq_status make_layout(const tq_config* cfg, tq_layout* out) {
   if (d != 128) return TQ_ERR_UNSUPPORTED;
   const int bs = cfg->block_size;
   if (bs != 16 && bs != 32 && bs != 64 && bs != 128) return TQ_ERR_UNSUPPORTED;
-  if (pi.value_bits != 4) return TQ_ERR_UNSUPPORTED;   // 3-bit values: not built yet
 
   tq_layout L;
   std::memset(&L, 0, sizeof(L));

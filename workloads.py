@@ -26,6 +26,7 @@ block_size = 16):
             chunk through a random slot mapping into 512 fresh blocks.
   long      4bit_nc, batch 4 x 131072, n_q 64 / n_kv 8; bf16 N(0,1) K, V with
             one channel per head drawn Student-t (nu = 3); 256 partitions of 512.
+  3bit      3bit_nc (3-bit keys and values) on the gqa shape and distributions.
 
 ``*_small`` variants keep the head structure and distributions with a few
 hundred tokens per sequence so the CPU oracle finishes in seconds.
@@ -88,6 +89,11 @@ WORKLOADS = {
                            store_tokens=300, store_extra_blocks=24, partition_tokens=128),
     "long_small": Workload("long_small", "4bit_nc", 2, 64, 8, lens=(1500, 333),
                            outlier="student_t", partition_tokens=256),
+    # 3bit_nc (3-bit keys and 3-bit values) on the gqa shape
+    "3bit": Workload("3bit", "3bit_nc", 32, 32, 8, fixed_len=4096, outlier="one_x8",
+                     note="batch 32 x ctx 4096, n_q 32, n_kv 8, 3-bit K and V"),
+    "3bit_small": Workload("3bit_small", "3bit_nc", 3, 32, 8, lens=(300, 517, 64),
+                           outlier="one_x8", partition_tokens=128),
 }
 
 

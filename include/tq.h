@@ -61,7 +61,10 @@ typedef enum {
   TQ_PRESET_K8V4 = 0,     /* K: e4m3, no rotation, no norm; V: 4-bit        */
   TQ_PRESET_4BIT_NC = 1,  /* K: 4-bit Lloyd-Max + norm correction; V: 4-bit */
   TQ_PRESET_K3V4_NC = 2,  /* K: 3-bit Lloyd-Max + norm correction; V: 4-bit */
-  TQ_PRESET_3BIT_NC = 3   /* K: 3-bit + norm correction; V: 3-bit           */
+  TQ_PRESET_3BIT_NC = 3,  /* K: 3-bit + norm correction; V: 3-bit           */
+  TQ_PRESET_PROD3 = 4     /* keys only: 2-bit Lloyd-Max code + 1-bit QJL residual
+                             sign per coordinate (TurboQuant_prod; the tq_prod_*
+                             entry points below, its own key cache)          */
 } tq_preset;
 
 typedef enum { TQ_DTYPE_F16 = 0, TQ_DTYPE_BF16 = 1, TQ_DTYPE_F32 = 2 } tq_dtype;
@@ -295,13 +298,84 @@ tq_status tq_dequant(const tq_config* cfg, const tq_codebook* cb,
                      void* key_out, void* value_out, int out_dtype,
                      unsigned int* dev_status, tq_stream_t stream);
 
+/* ---- TurboQuant_prod keys (QJL residual) -------------------------------
+ * The product-quantizer variant of the method: [vLLM-TQ] section "Lloyd-Max
+ * 量化器" (the TurboQuant_mse / TurboQuant_prod passage; vLLM itself ships only
+ * the MSE quantizer, section "TurboQuant 在 vLLM 中的位置", "为什么不用 QJL") and
+ * [TQ-proj] the page on the open-source turboquant project
+ * (kwkr.cn/news/555717), subsection "最后 1 bit 的巧思". For preset
+ * TQ_PRESET_PROD3 a key k of n_kv heads is stored as
+ *   n = ||k|| (fp16); y = (H / sqrt(d)) k / (n + 1e-8);
+ *   idx = 2-bit Lloyd-Max code of y (codebook tq_build_codebook(d, 2));
+ *   r = y - c[idx]; ||r|| (fp16); one bit per row i of S: (S r)_i >= 0
+ * and <q, k> is estimated, without bias over a Gaussian S, as
+ *   n * (<q_r, c[idx]> + ||r|| * sqrt(pi / 2) / d * <S q_r, signs>),
+ * q_r = (H / sqrt(d)) q, signs in {-1, +1}. S is an input: d x d fp32,
+ * row-major (row i is projection i), i.i.d. N(0, 1) entries drawn by the
+ * caller; the same S must serve the store and the scores.
+ *
+ * Key cache (keys only): cache[num_blocks][n_kv][block_size / 16][tile_bytes],
+ * a tile holding 16 positions of one KV head as regions: index streams
+ * (16 x k_row_bytes, LSB-first), sign streams (16 x sign_row_bytes, bit i of
+ * byte i / 8 is projection i), fp16 norms (16), fp16 residual norms (16). */
+typedef struct {
+  int mse_bits;           /* 2 */
+  int slot_bytes;         /* per (position, KV head): 52 at d = 128 */
+  int tile_bytes;         /* 16 * slot_bytes */
+  int k_off, k_row_bytes;
+  int sign_off, sign_row_bytes;
+  int norm_off, rnorm_off;
+  long long block_bytes;
+} tq_prod_layout;
+
+/* Host. The prod key cache layout of cfg (cfg->preset must be
+ * TQ_PRESET_PROD3; num_q_heads is not used). */
+tq_status tq_prod_layout_for(const tq_config* cfg, tq_prod_layout* out);
+
+/* Device. Quantise and write num_tokens keys into the prod key cache.
+ *   cb            host, tq_build_codebook(d, 2)
+ *   S             device fp32 [d][d], row-major, 16-byte aligned
+ *   key           device [num_tokens][n_kv][d], in_dtype f16 or bf16, 16-byte aligned
+ *   slot_mapping  device int64 [num_tokens]; slot < 0 writes nothing
+ *   cache         device, num_blocks * block_bytes, 16-byte aligned
+ *   dev_status    device uint32 or NULL (TQ_DEV_SLOT_OUT_OF_RANGE)
+ * Uses 129 KB of shared memory per CTA (S and a block of residuals). */
+tq_status tq_prod_store(const tq_config* cfg, const tq_codebook* cb, const float* S,
+                        const void* key, int in_dtype, long long num_tokens,
+                        const long long* slot_mapping, void* cache, long long num_blocks,
+                        unsigned int* dev_status, tq_stream_t stream);
+
+/* Host. Workspace bytes of tq_prod_scores: the rotated query and S times it,
+ * fp32, per (sequence, query head). 0 on bad input. */
+size_t tq_prod_scores_workspace_size(const tq_config* cfg, int batch);
+
+/* Device. scores[b][h][p] = scale * the estimate of <q[b][h], k_p> for every
+ * cached position p < min(seq_lens[b], max_seq_len, bt_stride * block_size)
+ * of sequence b, query head h reading KV head h / (n_q / n_kv); positions
+ * from there to max_seq_len are written as 0.
+ *   q            device [batch][n_q][d], q_dtype f16 or bf16, 16-byte aligned
+ *   cache, num_blocks, block_table, bt_stride, seq_lens, batch, max_seq_len
+ *                as for tq_decode (the prod key cache)
+ *   scale        <= 0 selects 1 / sqrt(d)
+ *   scores       device fp32 [batch][n_q][max_seq_len], 16-byte aligned
+ *   workspace    device, >= tq_prod_scores_workspace_size bytes, 16-byte aligned
+ *   dev_status   device uint32 or NULL (TQ_DEV_BLOCK_OUT_OF_RANGE,
+ *                TQ_DEV_SEQ_TOO_LONG; a bad block's positions score 0)
+ * Two launches: the query preparation, then the scores. */
+tq_status tq_prod_scores(const tq_config* cfg, const tq_codebook* cb, const float* S,
+                         const void* q, int q_dtype, const void* cache, long long num_blocks,
+                         const int* block_table, int bt_stride, const int* seq_lens, int batch,
+                         int max_seq_len, float scale, float* scores,
+                         void* workspace, size_t workspace_bytes,
+                         unsigned int* dev_status, tq_stream_t stream);
+
 /* Host. Static description of a status code. */
 const char* tq_status_string(int status);
 
 /* Host. ABI version of this header (major * 100 + minor). */
 int tq_version(void);
 
-#define TQ_ABI_VERSION 102   /* 1.01: tq_dequant added; 1.02: 3bit_nc (3-bit values) runs */
+#define TQ_ABI_VERSION 103   /* 1.01: tq_dequant; 1.02: 3bit_nc runs; 1.03: TurboQuant_prod (tq_prod_*) */
 
 #ifdef __cplusplus
 }

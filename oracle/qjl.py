@@ -65,12 +65,20 @@ def unpack_signs(packed: np.ndarray, d: int) -> np.ndarray:
     return 2.0 * b.astype(np.float64) - 1.0
 
 
-def prod_quantize(k: np.ndarray, S: np.ndarray, centroids: np.ndarray, midpoints: np.ndarray, mse_bits: int):
+def prod_quantize(k: np.ndarray, S: np.ndarray, centroids: np.ndarray, midpoints: np.ndarray, mse_bits: int,
+                  idx: np.ndarray | None = None):
     """Quantise rows of k [M, d] (float64 values of the inputs).
 
     Returns a dict: idx [M, d] (Lloyd-Max indices), norm [M] (float64 ||k||),
     rnorm [M] (float64 ||r||), proj [M, d] (float64 S r), sign_bits [M, d]
     ({0, 1}, 1 where S r >= 0), plus the packed forms and fp16 bit patterns.
+
+    ``idx`` [M, d], when given, replaces the nearest-centroid decision: the
+    residual, its norm and its signs are then those of that code. A
+    coordinate whose rotated value lies on a midpoint to within rounding may
+    be coded to either neighbour by an implementation computing in another
+    precision; this lets a comparison follow its choice instead of counting
+    the one flip again in every sign of the vector.
     """
     k = np.asarray(k, dtype=np.float64)
     S = np.asarray(S, dtype=np.float64)
@@ -78,7 +86,10 @@ def prod_quantize(k: np.ndarray, S: np.ndarray, centroids: np.ndarray, midpoints
     y = rotation.rotate(k / (n[:, None] + 1e-8))
     y32 = y.astype(np.float32)
     mids = np.asarray(midpoints, dtype=np.float32)
-    idx = (y32[:, :, None] >= mids[None, None, :]).sum(axis=-1).astype(np.int64)
+    if idx is None:
+        idx = (y32[:, :, None] >= mids[None, None, :]).sum(axis=-1).astype(np.int64)
+    else:
+        idx = np.asarray(idx, dtype=np.int64).reshape(y.shape)
     c = np.asarray(centroids, dtype=np.float32).astype(np.float64)
     r = y - c[idx]
     rnorm = np.sqrt((r * r).sum(axis=-1))

@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(tq):
     assert sorted(_abi.EXPORTED) == declared
     # matches the header's TQ_ABI_VERSION
     text = open(os.path.join(ROOT, "include", "tq.h")).read()
-    assert tq.tq_version() == int(re.search(r"#define TQ_ABI_VERSION (\d+)", text).group(1)) == 102
+    assert tq.tq_version() == int(re.search(r"#define TQ_ABI_VERSION (\d+)", text).group(1)) == 103
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
@@ -174,3 +174,62 @@ def test_dequant_binding_rejects_mixed_output_dtypes(tq):
     with pytest.raises(ValueError):
         tq.tq_dequant(cfg, cb, torch.empty(16), torch.zeros((1, 1), dtype=torch.int32),
                       torch.zeros(1, dtype=torch.int32), 16, k, v)
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+def test_prod_layout_equals_oracle(tq, bs):
+    from oracle import qjl
+    lay = tq.tq_prod_layout_for(tq.make_config("prod3", 32, 8, block_size=bs))
+    ref = qjl.prod_tile_layout(128, bs, 8, 2)
+    assert (lay.mse_bits, lay.tile_bytes, lay.slot_bytes) == (2, ref.tile_bytes, ref.slot_bytes)
+    assert (lay.k_off, lay.k_row_bytes, lay.sign_off, lay.sign_row_bytes) == (ref.k_off, ref.kb, ref.s_off, ref.sb)
+    assert (lay.norm_off, lay.rnorm_off, lay.block_bytes) == (ref.norm_off, ref.rnorm_off, ref.block_bytes)
+
+
+def test_prod_argument_errors_return_before_launch(tq):
+    from turboquant_paged_kv_gb300 import _abi
+    lib = _abi.load()
+    cfg = tq.make_config("prod3", 32, 8)
+    cb2 = tq.tq_build_codebook(128, 2)
+    cb4 = tq.tq_build_codebook(128, 4)
+    ok16 = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    lay = _abi.tq_layout()
+    # the prod preset has no K/V layout, and the K/V presets no prod layout
+    assert lib.tq_layout_for(ctypes.byref(cfg), ctypes.byref(lay)) == _abi.TQ_ERR_UNSUPPORTED
+    play = _abi.tq_prod_layout()
+    assert lib.tq_prod_layout_for(ctypes.byref(tq.make_config("4bit_nc", 32, 8)), ctypes.byref(play)) == \
+        _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_prod_layout_for(ctypes.byref(tq.make_config("prod3", 32, 8, head_dim=64)), ctypes.byref(play)) == \
+        _abi.TQ_ERR_UNSUPPORTED
+
+    def st(cb=cb2, S=ok16, key=ok16, dtype=1, n=5, slots=ok16, cache=ok16, status=None, cfg_=cfg):
+        return lib.tq_prod_store(ctypes.byref(cfg_), None if cb is None else ctypes.byref(cb), S, key, dtype, n,
+                                 slots, cache, 4, status, None)
+
+    assert st(S=None, key=None, slots=None, cache=None, n=0) == _abi.TQ_OK
+    assert st(cb=cb4) == _abi.TQ_ERR_INVALID_ARG
+    assert st(cb=None) == _abi.TQ_ERR_INVALID_ARG
+    assert st(S=None) == _abi.TQ_ERR_INVALID_ARG
+    assert st(dtype=2) == _abi.TQ_ERR_INVALID_ARG
+    assert st(S=odd) == _abi.TQ_ERR_MISALIGNED
+    assert st(key=odd) == _abi.TQ_ERR_MISALIGNED
+    assert st(slots=ctypes.c_void_p(0x10004)) == _abi.TQ_ERR_MISALIGNED
+    assert st(n=-1) == _abi.TQ_ERR_INVALID_ARG
+
+    def sc(cfg_=cfg, cb=cb2, S=ok16, q=ok16, cache=ok16, table=ok16, lens=ok16, batch=2, L=64, out=ok16,
+           ws=ok16, ws_bytes=None):
+        need = tq.tq_prod_scores_workspace_size(cfg_, batch)
+        return lib.tq_prod_scores(ctypes.byref(cfg_), None if cb is None else ctypes.byref(cb), S, q, 1, cache, 4,
+                                  table, 4, lens, batch, L, 0.0, out, ws, need if ws_bytes is None else ws_bytes,
+                                  None, None)
+
+    assert tq.tq_prod_scores_workspace_size(cfg, 2) == 2 * 32 * 2 * 128 * 4
+    assert sc(S=None, q=None, cache=None, table=None, lens=None, out=None, ws=None, batch=0) == _abi.TQ_OK
+    assert sc(ws_bytes=100) == _abi.TQ_ERR_WORKSPACE_TOO_SMALL
+    assert sc(cb=cb4) == _abi.TQ_ERR_INVALID_ARG
+    assert sc(out=None) == _abi.TQ_ERR_INVALID_ARG
+    assert sc(out=odd) == _abi.TQ_ERR_MISALIGNED
+    assert sc(table=ctypes.c_void_p(0x10002)) == _abi.TQ_ERR_MISALIGNED
+    assert sc(cfg_=tq.make_config("prod3", 32, 2)) == _abi.TQ_ERR_UNSUPPORTED     # 16 query heads per KV head
+    assert sc(cfg_=tq.make_config("prod3", 30, 8)) == _abi.TQ_ERR_INVALID_ARG

@@ -17,7 +17,7 @@ from . import _abi
 from ._abi import (PRESET_IDS, TQ_DEV_BLOCK_OUT_OF_RANGE, TQ_DEV_SEQ_TOO_LONG,  # noqa: F401
                    TQ_DECODE_NOALLOC_SCRATCH_BYTES, TQ_DEV_SLOT_OUT_OF_RANGE, TQ_DEV_TIMEOUT,
                    TQ_DTYPE_BF16, TQ_DTYPE_F16, TQ_DTYPE_F32, TQ_ERR_WORKSPACE_TOO_SMALL,
-                   TQError, tq_codebook, tq_config, tq_layout)
+                   TQError, tq_codebook, tq_config, tq_layout, tq_prod_layout)
 
 
 
@@ -34,7 +34,8 @@ _DTYPES = {torch.float16: TQ_DTYPE_F16, torch.bfloat16: TQ_DTYPE_BF16, torch.flo
 
 __all__ = ["make_config", "tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode",
            "tq_decode_partials", "tq_decode_reduce", "tq_decode_noalloc", "tq_decode_workspace_size",
-           "tq_dequant",
+           "tq_dequant", "tq_prod_layout_for", "tq_prod_store", "tq_prod_scores_workspace_size",
+           "tq_prod_scores",
            "tq_status_string",
            "tq_version", "TQError", "lib_path"]
 
@@ -166,3 +167,45 @@ def tq_dequant(cfg: tq_config, cb, cache: torch.Tensor, block_table: torch.Tenso
         ctypes.byref(cfg), _cb(cb), _ptr(cache), num_blocks, _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), seq_lens.shape[0], max_seq_len, _ptr(key_out), _ptr(value_out),
         _DTYPES[key_out.dtype], _ptr(dev_status), _stream(stream)))
+
+
+def tq_prod_layout_for(cfg: tq_config) -> tq_prod_layout:
+    lay = tq_prod_layout()
+    _abi.check("tq_prod_layout_for", _LIB.tq_prod_layout_for(ctypes.byref(cfg), ctypes.byref(lay)))
+    return lay
+
+
+def tq_prod_store(cfg: tq_config, cb, S: torch.Tensor, key: torch.Tensor, slot_mapping: torch.Tensor,
+                  cache: torch.Tensor, num_blocks: int | None = None, dev_status: torch.Tensor | None = None,
+                  stream=None) -> None:
+    """TurboQuant_prod keys: key [N, n_kv, d] f16/bf16, S fp32 [d, d] (row i =
+    projection i), slot_mapping [N] int64, cache uint8 (the prod key cache)."""
+    if S.dtype != torch.float32:
+        raise ValueError("S must be float32")
+    lay = tq_prod_layout_for(cfg)
+    if num_blocks is None:
+        num_blocks = cache.numel() // lay.block_bytes
+    _abi.check("tq_prod_store", _LIB.tq_prod_store(
+        ctypes.byref(cfg), _cb(cb), _ptr(S), _ptr(key), _DTYPES[key.dtype], key.shape[0], _ptr(slot_mapping),
+        _ptr(cache), num_blocks, _ptr(dev_status), _stream(stream)))
+
+
+def tq_prod_scores_workspace_size(cfg: tq_config, batch: int) -> int:
+    return int(_LIB.tq_prod_scores_workspace_size(ctypes.byref(cfg), batch))
+
+
+def tq_prod_scores(cfg: tq_config, cb, S: torch.Tensor, q: torch.Tensor, cache: torch.Tensor,
+                   block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int, scores: torch.Tensor,
+                   workspace: torch.Tensor, scale: float = 0.0, num_blocks: int | None = None,
+                   dev_status: torch.Tensor | None = None, stream=None) -> None:
+    """scores fp32 [B, n_q, max_seq_len]: scale * the unbiased estimate of <q, k_p>."""
+    if S.dtype != torch.float32 or scores.dtype != torch.float32:
+        raise ValueError("S and scores must be float32")
+    lay = tq_prod_layout_for(cfg)
+    if num_blocks is None:
+        num_blocks = cache.numel() // lay.block_bytes
+    _abi.check("tq_prod_scores", _LIB.tq_prod_scores(
+        ctypes.byref(cfg), _cb(cb), _ptr(S), _ptr(q), _DTYPES[q.dtype], _ptr(cache), num_blocks,
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, float(scale),
+        _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
+        _stream(stream)))

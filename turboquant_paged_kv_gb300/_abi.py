@@ -22,8 +22,9 @@ TQ_PRESET_K8V4 = 0
 TQ_PRESET_4BIT_NC = 1
 TQ_PRESET_K3V4_NC = 2
 TQ_PRESET_3BIT_NC = 3
+TQ_PRESET_PROD3 = 4
 PRESET_IDS = {"k8v4": TQ_PRESET_K8V4, "4bit_nc": TQ_PRESET_4BIT_NC,
-              "k3v4_nc": TQ_PRESET_K3V4_NC, "3bit_nc": TQ_PRESET_3BIT_NC}
+              "k3v4_nc": TQ_PRESET_K3V4_NC, "3bit_nc": TQ_PRESET_3BIT_NC, "prod3": TQ_PRESET_PROD3}
 
 TQ_DTYPE_F16 = 0
 TQ_DTYPE_BF16 = 1
@@ -37,7 +38,8 @@ TQ_DEV_TIMEOUT = 8
 # every function tq.h declares (checked by the ABI tests)
 EXPORTED = ("tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode_workspace_size",
             "tq_decode", "tq_decode_partials", "tq_decode_reduce", "tq_decode_noalloc",
-            "tq_dequant", "tq_status_string", "tq_version")
+            "tq_dequant", "tq_prod_layout_for", "tq_prod_store", "tq_prod_scores_workspace_size",
+            "tq_prod_scores", "tq_status_string", "tq_version")
 
 TQ_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -57,6 +59,13 @@ class tq_layout(ctypes.Structure):
                 ("v_off", ctypes.c_int), ("v_row_bytes", ctypes.c_int),
                 ("knorm_off", ctypes.c_int), ("vscale_off", ctypes.c_int), ("vzero_off", ctypes.c_int),
                 ("block_bytes", ctypes.c_longlong)]
+
+
+class tq_prod_layout(ctypes.Structure):
+    _fields_ = [("mse_bits", ctypes.c_int), ("slot_bytes", ctypes.c_int), ("tile_bytes", ctypes.c_int),
+                ("k_off", ctypes.c_int), ("k_row_bytes", ctypes.c_int),
+                ("sign_off", ctypes.c_int), ("sign_row_bytes", ctypes.c_int),
+                ("norm_off", ctypes.c_int), ("rnorm_off", ctypes.c_int), ("block_bytes", ctypes.c_longlong)]
 
 
 class tq_codebook(ctypes.Structure):
@@ -85,6 +94,12 @@ _SIGS = {
                                _vp, _i, _vp, _i, _i, _f, _vp, _i, _vp, _vp]),
     "tq_dequant": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_codebook), _vp, _ll, _vp, _i, _vp, _i,
                         _i, _vp, _vp, _i, _vp, _vp]),
+    "tq_prod_layout_for": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_prod_layout)]),
+    "tq_prod_store": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_codebook), _vp, _vp, _i, _ll, _vp, _vp, _ll,
+                           _vp, _vp]),
+    "tq_prod_scores_workspace_size": (_sz, [ctypes.POINTER(tq_config), _i]),
+    "tq_prod_scores": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_codebook), _vp, _vp, _i, _vp, _ll, _vp, _i,
+                            _vp, _i, _i, _f, _vp, _vp, _sz, _vp, _vp]),
     "tq_status_string": (ctypes.c_char_p, [_i]),
     "tq_version": (_i, []),
 }

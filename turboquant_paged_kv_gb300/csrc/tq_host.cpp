@@ -17,6 +17,7 @@ bool preset_info(int preset, PresetInfo* out) {
     case TQ_PRESET_4BIT_NC: *out = {4, 4, false, true}; return true;
     case TQ_PRESET_K3V4_NC: *out = {3, 4, false, true}; return true;
     case TQ_PRESET_3BIT_NC: *out = {3, 3, false, true}; return true;
+    case TQ_PRESET_PROD3:   *out = {2, 0, false, false}; return true;   // keys only: its own layout
     default: return false;
   }
 }
@@ -31,6 +32,7 @@ tq_status make_layout(const tq_config* cfg, tq_layout* out) {
   if (d != 128) return TQ_ERR_UNSUPPORTED;
   const int bs = cfg->block_size;
   if (bs != 16 && bs != 32 && bs != 64 && bs != 128) return TQ_ERR_UNSUPPORTED;
+  if (pi.value_bits == 0) return TQ_ERR_UNSUPPORTED;   // the prod preset has a key-only cache (tq_prod_layout_for)
 
   tq_layout L;
   std::memset(&L, 0, sizeof(L));

@@ -33,6 +33,7 @@
 
 #include "tq_internal.h"
 #include "tq_launch.cuh"
+#include "tq_vec.cuh"
 
 namespace tq {
 namespace {
@@ -64,61 +65,6 @@ struct StoreArgs {
 
 
 enum KeyMode { kMse4 = 4, kMse3 = 3, kFp8 = 8 };
-
-// 8 consecutive inputs (16 bytes) as floats.
-template <typename T>
-__device__ __forceinline__ void load8(const void* base, long long elem, float out[8]) {
-  const uint4 raw = ld_dep_u32x4(static_cast<const T*>(base) + elem);
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 f;
-    if constexpr (std::is_same<T, __nv_bfloat16>::value) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-    else f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-    out[2 * i] = f.x;
-    out[2 * i + 1] = f.y;
-  }
-}
-
-// Sum, min and max over the 16 lanes of a half-warp (xor 1 .. 8 stay inside it).
-__device__ __forceinline__ float half_sum(float x) {
-#pragma unroll
-  for (int m = 1; m <= 8; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-  return x;
-}
-__device__ __forceinline__ float half_min(float x) {
-#pragma unroll
-  for (int m = 1; m <= 8; m <<= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, m));
-  return x;
-}
-__device__ __forceinline__ float half_max(float x) {
-#pragma unroll
-  for (int m = 1; m <= 8; m <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, m));
-  return x;
-}
-
-// Sylvester-order Walsh-Hadamard transform (unnormalised) of the 128
-// coordinates of a half-warp, coordinate 8 l + j in lane l: index bits 0-2 in
-// the lane, bits 3-6 across lanes l ^ 1 .. l ^ 8. The lane whose stride bit is
-// set keeps (partner - own), the other (own + partner).
-__device__ __forceinline__ void fwht128_half(float v[8], int l) {
-#pragma unroll
-  for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      if (j & h) continue;
-      const float a = v[j], b = v[j + h];
-      v[j] = a + b;
-      v[j + h] = a - b;
-    }
-  }
-#pragma unroll
-  for (int m = 1; m <= 8; m <<= 1) {
-    const float sgn = (l & m) ? -1.f : 1.f;   // one exact fma with +-1 per step
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = fmaf(sgn, v[j], __shfl_xor_sync(0xffffffffu, v[j], m));
-  }
-}
 
 __device__ __forceinline__ void flag(unsigned int* status, unsigned int bit) {
   if (status) atomicOr(status, bit);

@@ -27,6 +27,9 @@ block_size = 16):
   long      4bit_nc, batch 4 x 131072, n_q 64 / n_kv 8; bf16 N(0,1) K, V with
             one channel per head drawn Student-t (nu = 3); 256 partitions of 512.
   3bit      3bit_nc (3-bit keys and values) on the gqa shape and distributions.
+  prod      prod3 keys (2-bit Lloyd-Max code + 1-bit QJL residual signs) on the
+            gqa shape and distributions; the QJL projection S is d x d
+            float32 N(0, 1) (``projection``).
 
 ``*_small`` variants keep the head structure and distributions with a few
 hundred tokens per sequence so the CPU oracle finishes in seconds.
@@ -38,10 +41,10 @@ from dataclasses import dataclass, field, replace
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "get", "Inputs"]
+__all__ = ["Workload", "WORKLOADS", "get", "Inputs", "make_inputs", "projection"]
 
 _KIND = {"q": 1, "k": 2, "v": 3, "lens": 4, "perm": 5, "slots": 6, "ch": 7,
-         "sk": 8, "sv": 9}
+         "sk": 8, "sv": 9, "proj": 10}
 
 
 @dataclass(frozen=True)
@@ -94,6 +97,10 @@ WORKLOADS = {
                      note="batch 32 x ctx 4096, n_q 32, n_kv 8, 3-bit K and V"),
     "3bit_small": Workload("3bit_small", "3bit_nc", 3, 32, 8, lens=(300, 517, 64),
                            outlier="one_x8", partition_tokens=128),
+    # TurboQuant_prod keys (key-only cache) on the gqa shape
+    "prod": Workload("prod", "prod3", 32, 32, 8, fixed_len=4096, outlier="one_x8",
+                     note="batch 32 x ctx 4096, n_q 32, n_kv 8, 2-bit code + QJL signs"),
+    "prod_small": Workload("prod_small", "prod3", 3, 32, 8, lens=(300, 517, 64), outlier="one_x8"),
 }
 
 
@@ -169,6 +176,12 @@ class Inputs:
         slots = torch.randperm(self.w.store_extra_blocks * self.w.block_size, generator=g)[:n]
         slots = (slots + first * self.w.block_size).to(torch.int64).to(device)
         return k, v, slots
+
+
+def projection(w: Workload, device="cpu") -> torch.Tensor:
+    """The QJL projection S [d, d] float32, i.i.d. N(0, 1) (row i = projection i)."""
+    g = _gen(w, "proj", 0, "cpu")
+    return torch.randn((w.d, w.d), generator=g, dtype=torch.float32).to(device)
 
 
 def make_inputs(w: Workload, device="cpu") -> Inputs:

@@ -224,7 +224,7 @@ def test_prod_argument_errors_return_before_launch(tq):
                                   table, 4, lens, batch, L, 0.0, out, ws, need if ws_bytes is None else ws_bytes,
                                   None, None)
 
-    assert tq.tq_prod_scores_workspace_size(cfg, 2) == 2 * 32 * 2 * 128 * 4
+    assert tq.tq_prod_scores_workspace_size(cfg, 2) == 2 * 8 * 32 * (32 + 12) * 4   # per KV head: 32 lanes x (32 operand words + 12 constants)
     assert sc(S=None, q=None, cache=None, table=None, lens=None, out=None, ws=None, batch=0) == _abi.TQ_OK
     assert sc(ws_bytes=100) == _abi.TQ_ERR_WORKSPACE_TOO_SMALL
     assert sc(cb=cb4) == _abi.TQ_ERR_INVALID_ARG
@@ -233,3 +233,6 @@ def test_prod_argument_errors_return_before_launch(tq):
     assert sc(table=ctypes.c_void_p(0x10002)) == _abi.TQ_ERR_MISALIGNED
     assert sc(cfg_=tq.make_config("prod3", 32, 2)) == _abi.TQ_ERR_UNSUPPORTED     # 16 query heads per KV head
     assert sc(cfg_=tq.make_config("prod3", 30, 8)) == _abi.TQ_ERR_INVALID_ARG
+    skew = tq.tq_build_codebook(128, 2)
+    skew.centroids[0] *= 1.5                   # not of the form {-A, -B, B, A}
+    assert sc(cb=skew) == _abi.TQ_ERR_INVALID_ARG

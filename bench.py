@@ -30,6 +30,7 @@ rotated between steps, so no step finds its cache in L2.
                   [--workload gqa|k3v4|k8v4|long|all] [--partition P]
   python bench.py --op dequant [--steps K] [--warmup W]   (full dequantisation alone)
   python bench.py --op store [--workload W]               (the prefill-chunk store alone)
+  python bench.py --op prod                               (TurboQuant_prod keys: scores + store)
 
 ``--impl reference`` times the CPU oracle (test infrastructure) on a bounded
 sample of the same workload. N > 1 runs weak-scaling replicas, one process
@@ -755,6 +756,132 @@ def run_store(args):
     return 0
 
 
+_PROD_ORACLE_SCRIPT = """
+import os, sys, time, json
+sys.path.insert(0, {root!r})
+import numpy as np, workloads
+from oracle import codebook as ocb
+from oracle import qjl
+w = workloads.get("prod", batch=1, fixed_len={tokens})
+inp = workloads.make_inputs(w)
+lay = qjl.prod_tile_layout(w.d, w.block_size, w.n_kv, 2)
+cent = ocb.codebook(w.d, 2)
+S = workloads.projection(w).double().numpy()
+cache = np.zeros(inp.num_blocks * lay.block_bytes, dtype=np.uint8)
+k = inp.kv_for_sequence(0, "cpu")[0].double().numpy()
+qjl.prod_store(k, inp.fill_slots.numpy(), S, cache, lay, cent, ocb.midpoints_fp32(cent))
+q = inp.q.double().numpy()
+times = []
+for _ in range({steps}):
+    t0 = time.perf_counter()
+    qjl.prod_scores(q, S, cache, lay, cent, inp.block_table.numpy(), inp.seq_lens.numpy(), {tokens})
+    times.append(time.perf_counter() - t0)
+print(json.dumps({{"times": times}}))
+"""
+PROD_ORACLE_TOKENS = 4096
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x fp32 lanes x FMA x max SM clock
+
+
+def run_prod(args):
+    """``--op prod``: the TurboQuant_prod key path (2-bit Lloyd-Max code + 1-bit
+    QJL residual signs) on the gqa shape, 32 x 4096 positions, n_q 32, n_kv 8:
+    each step is tq_prod_scores of every query head against every cached key
+    (a query-prep launch and the scores launch); four copies of the 54.5 MB
+    cache are rotated so no step finds its keys in L2. The line also carries
+    tq_prod_store of an 8192-token bf16 prefill chunk (bound by the fp32
+    projection S r) and the oracle's prod_scores on one whole sequence
+    (4096 positions). Prints one JSON line of its own."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from turboquant_paged_kv_gb300 import build as tqbuild
+    tqbuild.build()
+    import turboquant_paged_kv_gb300 as tq
+    import workloads
+
+    w = workloads.get("prod")
+    inp = workloads.make_inputs(w, device=dev)
+    cfg = tq.make_config("prod3", w.n_q, w.n_kv, block_size=w.block_size)
+    cb = tq.tq_build_codebook(w.d, 2)
+    lay = tq.tq_prod_layout_for(cfg)
+    S = workloads.projection(w, dev)
+    caches = [torch.empty(inp.num_blocks * lay.block_bytes, dtype=torch.uint8, device=dev) for _ in range(4)]
+    for b in range(w.batch):
+        k = inp.kv_for_sequence(b, dev)[0]
+        s0 = dict(inp.fill_order)[b]
+        tq.tq_prod_store(cfg, cb, S, k, inp.fill_slots[s0: s0 + k.shape[0]], caches[0])
+    for c in caches[1:]:
+        c.copy_(caches[0])
+    L = inp.max_seq_len
+    positions = int(inp.seq_lens.sum().item())
+    scores = torch.empty(w.batch, w.n_q, L, dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_prod_scores_workspace_size(cfg, w.batch), dtype=torch.uint8, device=dev)
+    nbytes = positions * w.n_kv * lay.slot_bytes + scores.numel() * 4 + inp.q.numel() * 2
+    stream = torch.cuda.current_stream()
+
+    def step(i=0):
+        tq.tq_prod_scores(cfg, cb, S, inp.q, caches[i % 4], inp.block_table, inp.seq_lens, L, scores, ws)
+
+    # store leg: an 8192-token prefill chunk through random distinct slots
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    nblk = 2 * STORE_TOKENS // w.block_size
+    kst = torch.randn(STORE_TOKENS, w.n_kv, w.d, generator=g, device=dev).to(torch.bfloat16)
+    sst = torch.randperm(nblk * w.block_size, generator=g, device=dev)[:STORE_TOKENS].to(torch.int64)
+    cst = torch.zeros(nblk * lay.block_bytes, dtype=torch.uint8, device=dev)
+
+    def store(_i=0):
+        tq.tq_prod_store(cfg, cb, S, kst, sst, cst)
+
+    for _ in range(args.warmup):
+        step()
+        store()
+    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else "0"
+    reps = max(args.steps, 100)
+    with ClockSampler(gpu_id) as clk:
+        ms = time_device(step, reps, stream)
+        ms_store = time_device(store, 20, stream)
+    peak, peak_src = _peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    store_tflops = STORE_TOKENS * w.n_kv * 2 * w.d * w.d / (ms_store * 1e-3) / 1e12
+    line = {
+        "op": "prod", "metric": "TurboQuant_prod scores GB/s (packed prod keys read + fp32 scores written); keys/s",
+        "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": reps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "f32 arithmetic, f16 query operands on tensor cores, bf16 in",
+        "data": "synthetic",
+        "config": {"workload": _workload_text(w), "l2": "4 cache copies of %.1f MB rotated" %
+                   (positions * w.n_kv * lay.slot_bytes / 1e6), "bytes_per_launch": nbytes},
+        "keys_per_s": positions * w.n_kv / (ms * 1e-3),
+        "roofline": {"kernel": "prod_query_kernel + prod_scores_kernel (one tq_prod_scores call)", "bound": "hbm",
+                     "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src,
+                     "ms_per_launch": ms, "algorithmic_bytes_per_launch": nbytes,
+                     "traffic": _profile_field("tq_prod.cu", "prod_scores_prod.md", "dram_bytes_per_launch")},
+        "store": {"kernel": "prod_store_kernel (tq_prod_store)", "tokens": STORE_TOKENS,
+                  "mtok_s": STORE_TOKENS / (ms_store * 1e-3) / 1e6, "ms_per_launch": ms_store,
+                  "roofline": {"bound": "alu", "achieved": store_tflops, "peak": FP32_PEAK_TFLOPS,
+                               "unit": "TFLOP/s", "frac": store_tflops / FP32_PEAK_TFLOPS,
+                               "peak_source": "derived: 152 SMs x 128 fp32 FMA/clk x 2 x 2070 MHz",
+                               "flops_per_launch": STORE_TOKENS * w.n_kv * 2 * w.d * w.d}},
+        "gpu_launches": 2 * reps + 20,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        code = _PROD_ORACLE_SCRIPT.format(root=ROOT, tokens=PROD_ORACLE_TOKENS, steps=30)
+        out = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **_SINGLE_THREAD_ENV),
+                             capture_output=True, text=True, check=True).stdout
+        t = statistics.mean(json.loads(out.strip().splitlines()[-1])["times"][1:])
+        obytes = PROD_ORACLE_TOKENS * w.n_kv * lay.slot_bytes + w.n_q * PROD_ORACLE_TOKENS * 4
+        line["cpu_baseline"] = {"value": obytes / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "keys_per_s": PROD_ORACLE_TOKENS * w.n_kv / t,
+                                "sample": f"1 sequence x {PROD_ORACLE_TOKENS} positions, 8 KV heads x 4 query "
+                                          "heads each: oracle prod_scores"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -766,9 +893,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dry-run", action="store_true",
                     help="run the multi-rank host logic on the CPU (gloo) without a GPU")
-    ap.add_argument("--op", default="decode", choices=["decode", "dequant", "store"],
+    ap.add_argument("--op", default="decode", choices=["decode", "dequant", "store", "prod"],
                     help="decode: the decode step (default); dequant: tq_dequant of the gqa cache alone; "
-                         "store: tq_store of the workload's prefill chunk alone")
+                         "store: tq_store of the workload's prefill chunk alone; prod: the TurboQuant_prod "
+                         "key path (scores + store)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -790,6 +918,8 @@ def main(argv=None):
         return run_dequant(args)
     if args.op == "store":
         return run_store(args)
+    if args.op == "prod":
+        return run_prod(args)
     return run_reference(args) if args.impl == "reference" else run_tq(args)
 
 

@@ -298,6 +298,63 @@ tq_status tq_dequant(const tq_config* cfg, const tq_codebook* cb,
                      void* key_out, void* value_out, int out_dtype,
                      unsigned int* dev_status, tq_stream_t stream);
 
+/* ---- continuation chunks ---------------------------------------------
+ * A prefill chunk of new tokens whose keys and values are already stored
+ * (tq_store) attends to its sequence's cached history and to itself,
+ * causally: [vLLM-TQ] section "续写 prefill:小 chunk 走 decode,大 chunk 走反量化"
+ * (a chunk of at most 128 tokens is served by the decode kernel, query i as a
+ * request of length cached + i + 1 over the sequence's block-table row). The
+ * result equals tq_decode run once per query with those lengths; here one CTA
+ * serves 64 / G queries of a KV head per pass over the history (G = n_q /
+ * n_kv, which must divide 8), so the history is read ceil(q_len * G / 64)
+ * times instead of q_len times.
+ *
+ * Host. Workspace bytes for `total_q` query rows whose sequences are at most
+ * max_seq_len long: one record (d fp32 + an LSE) per (query, query head,
+ * partition of partition_tokens positions, default 512). 0 for an invalid
+ * config. */
+size_t tq_continue_workspace_size(const tq_config* cfg, int total_q, int max_seq_len);
+
+/* Device.
+ *   cfg, cb       host; as for tq_decode (G = n_q / n_kv in {1, 2, 4, 8};
+ *                 partition_tokens a multiple of 16 up to 4096, 0 = 512)
+ *   q, q_dtype    device [total_q][n_q][d] f16 or bf16, 16-byte aligned: the
+ *                 chunks' queries, sequence b's in rows
+ *                 query_start[b] .. query_start[b + 1] - 1
+ *   query_start   device int32 [batch + 1], non-decreasing, query_start[0] = 0
+ *                 and query_start[batch] = total_q
+ *   max_q_len     host; the longest chunk (rows of a longer chunk past
+ *                 max_q_len are not served: they come out 0 and flag
+ *                 TQ_DEV_SEQ_TOO_LONG)
+ *   cache, num_blocks, block_table, bt_stride
+ *                 as for tq_decode; row b of block_table is sequence b's
+ *   seq_lens      device int32 [batch]: each sequence's length with its chunk
+ *                 (query i of a chunk of q_len sits at position
+ *                 seq_lens[b] - q_len + i and sees positions 0 .. that one)
+ *   max_seq_len   host; >= every seq_lens[b] (sizes the partitions)
+ *   scale         softmax scale; <= 0 means 1 / sqrt(d)
+ *   out, out_dtype  device [total_q][n_q][d] f16, bf16 or f32, 16-byte
+ *                 aligned, owned by the caller; every row is written (a
+ *                 query that sees no position gives 0)
+ *   workspace     device, >= tq_continue_workspace_size(cfg, total_q,
+ *                 max_seq_len) bytes, 16-byte aligned, owned by the caller
+ *   dev_status    device uint32 or NULL: TQ_DEV_SEQ_TOO_LONG for a length
+ *                 above bt_stride * block_size or a chunk past max_q_len or
+ *                 total_q, TQ_DEV_BLOCK_OUT_OF_RANGE for a bad block id (its
+ *                 positions are skipped)
+ * batch == 0, total_q == 0 or max_q_len == 0 is a no-op. Two launches: the
+ * attention kernel (grid n_kv * ceil(max_q_len * G / 64) x partitions x
+ * batch) and a reduce over the partitions. */
+tq_status tq_continue(const tq_config* cfg, const tq_codebook* cb,
+                      const void* q, int q_dtype,
+                      const int* query_start, int batch, int total_q, int max_q_len,
+                      const void* cache, long long num_blocks,
+                      const int* block_table, int bt_stride,
+                      const int* seq_lens, int max_seq_len, float scale,
+                      void* out, int out_dtype,
+                      void* workspace, size_t workspace_bytes,
+                      unsigned int* dev_status, tq_stream_t stream);
+
 /* ---- TurboQuant_prod keys (QJL residual) -------------------------------
  * The product-quantizer variant of the method: [vLLM-TQ] section "Lloyd-Max
  * 量化器" (the TurboQuant_mse / TurboQuant_prod passage; vLLM itself ships only
@@ -375,7 +432,8 @@ const char* tq_status_string(int status);
 /* Host. ABI version of this header (major * 100 + minor). */
 int tq_version(void);
 
-#define TQ_ABI_VERSION 103   /* 1.01: tq_dequant; 1.02: 3bit_nc runs; 1.03: TurboQuant_prod (tq_prod_*) */
+#define TQ_ABI_VERSION 104   /* 1.01: tq_dequant; 1.02: 3bit_nc runs; 1.03: TurboQuant_prod (tq_prod_*);
+                                 1.04: tq_continue */
 
 #ifdef __cplusplus
 }

@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(tq):
     assert sorted(_abi.EXPORTED) == declared
     # matches the header's TQ_ABI_VERSION
     text = open(os.path.join(ROOT, "include", "tq.h")).read()
-    assert tq.tq_version() == int(re.search(r"#define TQ_ABI_VERSION (\d+)", text).group(1)) == 103
+    assert tq.tq_version() == int(re.search(r"#define TQ_ABI_VERSION (\d+)", text).group(1)) == 104
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
@@ -236,3 +236,38 @@ def test_prod_argument_errors_return_before_launch(tq):
     skew = tq.tq_build_codebook(128, 2)
     skew.centroids[0] *= 1.5                   # not of the form {-A, -B, B, A}
     assert sc(cb=skew) == _abi.TQ_ERR_INVALID_ARG
+
+
+def test_continue_workspace_and_argument_errors(tq):
+    from turboquant_paged_kv_gb300 import _abi
+    lib = _abi.load()
+    cfg = tq.make_config("4bit_nc", 32, 8)
+    # one record (d floats + an LSE) per (query, query head, 512-position partition)
+    assert tq.tq_continue_workspace_size(cfg, 128, 4224) == 128 * 32 * 9 * 129 * 4
+    assert tq.tq_continue_workspace_size(tq.make_config("4bit_nc", 32, 8, partition_tokens=128), 3, 300) == \
+        (3 * 32 * 3 * 129 * 4 + 15) // 16 * 16
+    assert tq.tq_continue_workspace_size(tq.make_config("4bit_nc", 24, 8), 4, 64) == 0        # G = 3
+    assert tq.tq_continue_workspace_size(tq.make_config("4bit_nc", 32, 8, partition_tokens=8192), 4, 64) == 0
+    cb = tq.tq_build_codebook(128, 4)
+    cb3 = tq.tq_build_codebook(128, 3)
+    ok16 = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+
+    def cont(cfg_=cfg, cb_=cb, q=ok16, qs=ok16, batch=2, total=10, mql=8, cache=ok16, table=ok16, lens=ok16,
+             out=ok16, ws=ok16, ws_bytes=None, qd=1, od=2):
+        need = tq.tq_continue_workspace_size(cfg_, total, 64)
+        return lib.tq_continue(ctypes.byref(cfg_), None if cb_ is None else ctypes.byref(cb_), q, qd, qs, batch,
+                               total, mql, cache, 10, table, 4, lens, 64, 0.0, out, od, ws,
+                               need if ws_bytes is None else ws_bytes, None, None)
+
+    assert cont(q=None, qs=None, cache=None, table=None, lens=None, out=None, ws=None, total=0) == _abi.TQ_OK
+    assert cont(q=None, qs=None, cache=None, table=None, lens=None, out=None, ws=None, batch=0) == _abi.TQ_OK
+    assert cont(ws_bytes=64) == _abi.TQ_ERR_WORKSPACE_TOO_SMALL
+    assert cont(cb_=cb3) == _abi.TQ_ERR_INVALID_ARG
+    assert cont(qd=2) == _abi.TQ_ERR_INVALID_ARG
+    assert cont(od=7) == _abi.TQ_ERR_INVALID_ARG
+    assert cont(qs=None) == _abi.TQ_ERR_INVALID_ARG
+    assert cont(out=odd) == _abi.TQ_ERR_MISALIGNED
+    assert cont(qs=ctypes.c_void_p(0x10002)) == _abi.TQ_ERR_MISALIGNED
+    assert cont(cfg_=tq.make_config("4bit_nc", 24, 8)) == _abi.TQ_ERR_UNSUPPORTED
+    assert cont(batch=-1) == _abi.TQ_ERR_INVALID_ARG

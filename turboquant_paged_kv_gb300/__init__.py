@@ -35,7 +35,7 @@ _DTYPES = {torch.float16: TQ_DTYPE_F16, torch.bfloat16: TQ_DTYPE_BF16, torch.flo
 __all__ = ["make_config", "tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode",
            "tq_decode_partials", "tq_decode_reduce", "tq_decode_noalloc", "tq_decode_workspace_size",
            "tq_dequant", "tq_prod_layout_for", "tq_prod_store", "tq_prod_scores_workspace_size",
-           "tq_prod_scores",
+           "tq_prod_scores", "tq_continue_workspace_size", "tq_continue",
            "tq_status_string",
            "tq_version", "TQError", "lib_path"]
 
@@ -209,3 +209,24 @@ def tq_prod_scores(cfg: tq_config, cb, S: torch.Tensor, q: torch.Tensor, cache: 
         _ptr(block_table), block_table.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, float(scale),
         _ptr(scores), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
         _stream(stream)))
+
+
+def tq_continue_workspace_size(cfg: tq_config, total_q: int, max_seq_len: int) -> int:
+    return int(_LIB.tq_continue_workspace_size(ctypes.byref(cfg), total_q, max_seq_len))
+
+
+def tq_continue(cfg: tq_config, cb, q: torch.Tensor, query_start: torch.Tensor, max_q_len: int,
+                cache: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                out: torch.Tensor, workspace: torch.Tensor, scale: float = 0.0, num_blocks: int | None = None,
+                dev_status: torch.Tensor | None = None, stream=None) -> None:
+    """Causal attention of continuation chunks: q [total_q, n_q, d], query_start
+    int32 [batch + 1], seq_lens int32 [batch] (lengths with the chunk),
+    block_table int32 [batch, stride], out [total_q, n_q, d]."""
+    lay = tq_layout_for(cfg)
+    if num_blocks is None:
+        num_blocks = cache.numel() // lay.block_bytes
+    _abi.check("tq_continue", _LIB.tq_continue(
+        ctypes.byref(cfg), _cb(cb), _ptr(q), _DTYPES[q.dtype], _ptr(query_start), seq_lens.shape[0], q.shape[0],
+        max_q_len, _ptr(cache), num_blocks, _ptr(block_table), block_table.shape[1], _ptr(seq_lens), max_seq_len,
+        float(scale), _ptr(out), _DTYPES[out.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream)))

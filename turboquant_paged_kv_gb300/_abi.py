@@ -39,7 +39,7 @@ TQ_DEV_TIMEOUT = 8
 EXPORTED = ("tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode_workspace_size",
             "tq_decode", "tq_decode_partials", "tq_decode_reduce", "tq_decode_noalloc",
             "tq_dequant", "tq_prod_layout_for", "tq_prod_store", "tq_prod_scores_workspace_size",
-            "tq_prod_scores", "tq_status_string", "tq_version")
+            "tq_prod_scores", "tq_continue_workspace_size", "tq_continue", "tq_status_string", "tq_version")
 
 TQ_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -100,6 +100,9 @@ _SIGS = {
     "tq_prod_scores_workspace_size": (_sz, [ctypes.POINTER(tq_config), _i]),
     "tq_prod_scores": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_codebook), _vp, _vp, _i, _vp, _ll, _vp, _i,
                             _vp, _i, _i, _f, _vp, _vp, _sz, _vp, _vp]),
+    "tq_continue_workspace_size": (_sz, [ctypes.POINTER(tq_config), _i, _i]),
+    "tq_continue": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_codebook), _vp, _i, _vp, _i, _i, _i, _vp, _ll,
+                         _vp, _i, _vp, _i, _f, _vp, _i, _vp, _sz, _vp, _vp]),
     "tq_status_string": (ctypes.c_char_p, [_i]),
     "tq_version": (_i, []),
 }

@@ -31,6 +31,7 @@ rotated between steps, so no step finds its cache in L2.
   python bench.py --op dequant [--steps K] [--warmup W]   (full dequantisation alone)
   python bench.py --op store [--workload W]               (the prefill-chunk store alone)
   python bench.py --op prod                               (TurboQuant_prod keys: scores + store)
+  python bench.py --op continue                           (128-query continuation chunks vs per-query decode)
 
 ``--impl reference`` times the CPU oracle (test infrastructure) on a bounded
 sample of the same workload. N > 1 runs weak-scaling replicas, one process
@@ -72,6 +73,15 @@ def _peaks():
         return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
     except Exception:
         return 6800.0, "fallback (6.8 TB/s)"
+
+
+def _tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst cuBLAS bf16 GEMM)"
+    except Exception:
+        return 1900.0, "fallback (1.9 PFLOP/s bf16 burst)"
 
 
 def _profile_field(kernel_file: str, summary: str, field: str):
@@ -882,6 +892,111 @@ def run_prod(args):
     return 0
 
 
+CONT_CHUNK = 128
+
+
+def run_continue(args):
+    """``--op continue``: continuation chunks. 32 sequences, each a 4096-token
+    cached history plus a 128-token chunk already stored (4224 positions, gqa
+    heads: n_q 32, n_kv 8, 4bit_nc; 145 MB of packed slots, above L2), served
+    by tq_continue (each KV tile read once per 64 / G = 16 queries) and, for
+    comparison, by the per-query path: tq_decode with 4096 requests of lengths
+    4097 .. 4224. Prints one JSON line of its own."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from turboquant_paged_kv_gb300 import build as tqbuild
+    tqbuild.build()
+    import turboquant_paged_kv_gb300 as tq
+    import workloads
+
+    base = workloads.get(DEFAULT_WORKLOAD)
+    w = workloads.get(DEFAULT_WORKLOAD, fixed_len=base.fixed_len + CONT_CHUNK)
+    inp = workloads.make_inputs(w, device=dev)
+    cfg = tq.make_config(w.preset, w.n_q, w.n_kv, block_size=w.block_size)
+    cb = tq.tq_build_codebook(w.d, 4)
+    lay = tq.tq_layout_for(cfg)
+    cache = torch.empty(inp.num_blocks * lay.block_bytes, dtype=torch.uint8, device=dev)
+    for b in range(w.batch):
+        k, v = inp.kv_for_sequence(b, dev)
+        s0 = dict(inp.fill_order)[b]
+        tq.tq_store(cfg, cb, k, v, inp.fill_slots[s0: s0 + k.shape[0]], cache)
+    L = inp.max_seq_len
+    total = w.batch * CONT_CHUNK
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    q = torch.randn(total, w.n_q, w.d, generator=g, device=dev).to(torch.bfloat16)
+    qs = (torch.arange(w.batch + 1, dtype=torch.int32, device=dev) * CONT_CHUNK)
+    out = torch.empty(total, w.n_q, w.d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(tq.tq_continue_workspace_size(cfg, total, L), dtype=torch.uint8, device=dev)
+    # per-query path: one decode request per chunk query
+    lens_pq = (torch.arange(CONT_CHUNK, dtype=torch.int32, device=dev) + (L - CONT_CHUNK + 1)).repeat(w.batch)
+    table_pq = inp.block_table.repeat_interleave(CONT_CHUNK, dim=0).contiguous()
+    out_pq = torch.empty_like(out)
+    ws_pq = torch.empty(tq.tq_decode_workspace_size(cfg, total, L), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def cont(_i=0):
+        tq.tq_continue(cfg, cb, q, qs, CONT_CHUNK, cache, inp.block_table, inp.seq_lens, L, out, ws)
+
+    def per_query(_i=0):
+        tq.tq_decode(cfg, cb, q, cache, table_pq, lens_pq, L, out_pq, ws_pq)
+
+    for _ in range(args.warmup):
+        cont()
+        per_query()
+    torch.cuda.synchronize()
+    err = (out.float() - out_pq.float()).abs().max().item()
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else "0"
+    reps = max(args.steps, 50)
+    with ClockSampler(gpu_id) as clk:
+        ms = time_device(cont, reps, stream)
+        ms_pq = time_device(per_query, max(reps // 10, 5), stream)
+    peak, peak_src = _peaks()
+    slot_bytes = w.n_kv * lay.slot_bytes
+    unique = w.batch * L * slot_bytes                              # every cached slot once
+    G = w.n_q // w.n_kv
+    passes = -(-CONT_CHUNK * G // 64)                              # query groups of 64 / G queries
+    cont_reads = sum(w.batch * min(L, L - CONT_CHUNK + min(CONT_CHUNK, 64 // G * (i + 1))) * slot_bytes
+                     for i in range(passes))
+    pq_reads = w.batch * sum(L - CONT_CHUNK + 1 + i for i in range(CONT_CHUNK)) * slot_bytes
+    gbs = unique / (ms * 1e-3) / 1e9
+    # algorithmic tensor work: every (query, query head) against every position it sees,
+    # d multiply-adds for the score and d for the output (2 flops each)
+    seen = w.batch * sum(L - CONT_CHUNK + 1 + i for i in range(CONT_CHUNK))
+    flops = seen * w.n_q * w.d * 4
+    tflops = flops / (ms * 1e-3) / 1e12
+    tpeak, tpeak_src = _tensor_peak()
+    print(json.dumps({
+        "op": "continue", "metric": "continuation chunk queries/s (128-query chunks over 4096-token histories)",
+        "value": total / (ms * 1e-3), "unit": "queries/s", "n_gpus": 1, "steps": reps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "dtype": "f32 softmax/accumulate, f16 tensor-core operands, bf16 in/out",
+        "data": "synthetic",
+        "config": {"workload": _workload_text(w, f", last {CONT_CHUNK} positions of each sequence are the chunk"),
+                   "l2": "the packed cache is %.0f MB (> L2)" % (unique / 1e6)},
+        "per_query_path": {"ms_per_step": ms_pq, "queries_per_s": total / (ms_pq * 1e-3),
+                           "kernel": "tq_decode, one request per chunk query", "speedup_of_continue": ms_pq / ms,
+                           "max_abs_diff_vs_continue": err},
+        "kv_bytes_read": {"continue": cont_reads, "per_query": pq_reads, "unique": unique,
+                          "ratio": pq_reads / cont_reads},
+        "roofline": {"kernel": "cont_kernel + cont_reduce_kernel (one tq_continue call)", "bound": "tensor",
+                     "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
+                     "peak_source": tpeak_src, "ms_per_launch": ms, "algorithmic_flops_per_launch": flops,
+                     "note": "flops = (query, query head) x visible position x d x 4 (QK and PV multiply-adds); "
+                             "mma.sync f16 operands with fp16 hi/lo query and probability parts, so the tensor "
+                             "pipe does twice the algorithmic work",
+                     "traffic": _profile_field("tq_continue.cu", "continue_gqa.md", "dram_bytes_per_launch"),
+                     "hbm": {"achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                             "bytes": unique, "note": "every packed slot once; the kernel reads the history "
+                                                      f"{passes} times (once per query group), the repeats from L2"}},
+        "gpu_launches": 2 * reps + 2 * max(reps // 10, 5),
+        "clocks": clk.summary(),
+    }), flush=True)
+    return 0
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -893,10 +1008,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dry-run", action="store_true",
                     help="run the multi-rank host logic on the CPU (gloo) without a GPU")
-    ap.add_argument("--op", default="decode", choices=["decode", "dequant", "store", "prod"],
+    ap.add_argument("--op", default="decode", choices=["decode", "dequant", "store", "prod", "continue"],
                     help="decode: the decode step (default); dequant: tq_dequant of the gqa cache alone; "
                          "store: tq_store of the workload's prefill chunk alone; prod: the TurboQuant_prod "
-                         "key path (scores + store)")
+                         "key path (scores + store); continue: 128-query continuation chunks")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -920,6 +1035,8 @@ def main(argv=None):
         return run_store(args)
     if args.op == "prod":
         return run_prod(args)
+    if args.op == "continue":
+        return run_continue(args)
     return run_reference(args) if args.impl == "reference" else run_tq(args)
 
 

@@ -45,6 +45,7 @@ struct DequantArgs {
   long long num_blocks;
   int n_kv;
   int max_seq_len;
+  int batch;
   int len_cap;               // min(max_seq_len, bt_stride * block_size)
   int seq_tiles;             // ceil(max_seq_len / 16): CTAs per (sequence, KV head)
   int bt_stride;
@@ -214,8 +215,288 @@ dequant_kernel(const DequantArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- tensor-core form
+//
+// Index-coded keys, a warp per (sequence, 16-position tile, KV head). The
+// inverse rotation H / sqrt(128) is a Kronecker product: with the 7 bits of a
+// coordinate split into R = {0, 1, 5, 6} and S = {2, 3, 4},
+//   H[a][b] = (-1)^popc(a & b) = H_R[a_R][b_R] * H_S[a_S][b_S],
+// so the 16 x 128 tile of rotated-basis keys C (rows: positions, C = c[idx])
+// is multiplied by H_R on tensor cores, one m16n8k16 per (S-block, 8 output
+// columns), and by H_S with a 3-stage butterfly over the 8 S-blocks held in
+// registers. Lane (g, t) holds the key bytes of rows g and g + 8 for
+// coordinates 32 t .. 32 t + 31, which is the decode's QK operand layout: in
+// S-block s its operand pairs are coordinates 32 t + 4 s + {0, 1} and
+// + {2, 3}, so the mma's k index kappa = e0 + 2 t + 8 e1 stands for a_R bits
+// (a0 = e0, a5 a6 = t, a1 = e1). The centroids enter as fp16 hi + lo parts
+// from a LUT (one 8-byte entry per key byte: both parts of both centroids, 32
+// copies so lookups never conflict), the H_R entries as exact fp16 +-1; the
+// only roundings are fp32 sums. Output column n = x + 2 t + 8 nt of S-block
+// s' is coordinate b = x + 2 (t & 1) + 32 (t >> 1) + 64 nt + 4 s'. Results
+// are multiplied by stored_norm / sqrt(128), staged per warp in shared memory
+// and written back as full rows. Values are expanded in the same pass with a
+// row-major lane map (lane: token pair lane >> 2, coordinates 8 (lane & 3) +
+// 32 k), so their 16-byte stores cover whole sectors.
+constexpr int kMmaWarps = 16;
+
+template <int KMODE>
+__host__ __device__ constexpr int lut_entries() { return KMODE == kMse4 ? 256 : 64; }
+
+// LUT entry index of operand step `st` (coordinates 32 t + 2 st, + 1) of this
+// lane's key slice kq: a key byte (4-bit keys) or a 6-bit pair (3-bit keys).
+template <int KMODE>
+__device__ __forceinline__ uint32_t key_entry(const uint4& kq, int st) {
+  const uint32_t w[4] = {kq.x, kq.y, kq.z, kq.w};
+  if constexpr (KMODE == kMse4) {
+    return (w[st >> 2] >> (8 * (st & 3))) & 0xFFu;
+  } else {
+    const int bit = 6 * st, wi = bit >> 5, sh = bit & 31;
+    const uint32_t f = sh <= 26 ? (w[wi] >> sh) : __funnelshift_r(w[wi], w[wi + 1], sh);
+    return f & 0x3Fu;
+  }
+}
+
+__device__ __forceinline__ void mma16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    const __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&t);
+  } else {
+    const __half2 t = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&t);
+  }
+}
+
+// The 8-byte value words of token pair `pair` that hold, for both tokens,
+// the codes of coordinates 8 l .. 8 l + 7 (as the row-major kernel reads them).
+template <int VBITS>
+__device__ __forceinline__ uint2 value_pair_words(const uint8_t* tile, const DequantArgs& a, int pair, int l) {
+  if constexpr (VBITS == 4) {
+    const int swz = (a.v_row % 64 == 0) ? 2 * (pair & 3) : 0;
+    return ld_dep_u32x2(tile + a.v_off + pair * 2 * a.v_row + 16 * ((l >> 1) ^ swz) + 8 * (l & 1));
+  } else {
+    const int w0 = 3 * (l >> 1) + (l & 1);
+    const uint8_t* pw = tile + a.v_off + pair * 2 * a.v_row + 4 * w0;
+    return make_uint2(ld_dep_u32(pw), ld_dep_u32(pw + 4));
+  }
+}
+
+// Codes of coordinates 8 l .. 8 l + 7 of token j (0, 1) of the pair, LSB first.
+template <int VBITS>
+__device__ __forceinline__ uint32_t token_codes(uint2 vw, int j, int l) {
+  const int sh = 16 * j;
+  if constexpr (VBITS == 4) {
+    return ((vw.x >> sh) & 0xFFFFu) | (((vw.y >> sh) & 0xFFFFu) << 16);
+  } else {
+    return (((vw.x >> sh) & 0xFFFFu) | (((vw.y >> sh) & 0xFFFFu) << 16)) >> (8 * (l & 1));
+  }
+}
+
+template <int KMODE, int VBITS, typename T>
+__global__ void __launch_bounds__(kMmaWarps * 32, 1) dequant_mma_kernel(const DequantArgs a) {
+  extern __shared__ __align__(16) uint8_t s_dq[];
+  constexpr int kRow = kD * static_cast<int>(sizeof(T)) + 16;   // staging row stride (bytes)
+  uint2* lut = reinterpret_cast<uint2*>(s_dq);                   // [entry][lane]: (hi, lo) half2 pair
+  grid_dep_wait();   // cache, tables and lengths may come from the previous kernel
+  grid_dep_launch();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
+  uint8_t* stage = s_dq + lut_entries<KMODE>() * 32 * 8 + warp * 16 * kRow;
+  constexpr int kShift = KMODE == kMse4 ? 4 : 3;
+  for (int i = tid; i < lut_entries<KMODE>() * 32; i += blockDim.x) {
+    const int e = i >> 5;
+    const float c0 = a.cent[e & ((1 << kShift) - 1)], c1 = a.cent[e >> kShift];
+    const __half h0 = __float2half_rn(c0), h1 = __float2half_rn(c1);
+    const __half l0 = __float2half_rn(c0 - __half2float(h0)), l1 = __float2half_rn(c1 - __half2float(h1));
+    lut[i] = make_uint2(static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16),
+                        static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16));
+  }
+  // B operands: H_R[kappa][n] = (-1)^(k0 n0 + k3 n1 + k1 n2 + k2 n3), kappa = 2 t + {0, 1} (+ 8), n = 8 nt + g
+  uint32_t hb[2][2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int k = 2 * t + x + 8 * r, n = 8 * nt + g;
+        const int par = ((k & 1) & (n & 1)) ^ (((k >> 3) & 1) & ((n >> 1) & 1)) ^ (((k >> 1) & 1) & ((n >> 2) & 1)) ^
+                        (((k >> 2) & 1) & ((n >> 3) & 1));
+        v |= (par ? 0xBC00u : 0x3C00u) << (16 * x);
+      }
+      hb[nt][r] = v;
+    }
+  }
+  __syncthreads();   // LUT
+
+  // tiles in (sequence, tile, KV head) order, so neighbouring warps write neighbouring output rows
+  const unsigned total = static_cast<unsigned>(a.seq_tiles) * static_cast<unsigned>(a.batch) * static_cast<unsigned>(a.n_kv);
+  const unsigned nwarps = gridDim.x * kMmaWarps;
+  for (unsigned u = blockIdx.x * kMmaWarps + warp; u < total; u += nwarps) {
+    const unsigned bt = u / static_cast<unsigned>(a.n_kv);
+    const int h = static_cast<int>(u - bt * static_cast<unsigned>(a.n_kv));
+    const int b = static_cast<int>(bt / static_cast<unsigned>(a.seq_tiles));
+    const int tl = static_cast<int>(bt - static_cast<unsigned>(b) * static_cast<unsigned>(a.seq_tiles));
+    const int raw_len = ld_dep_s32(a.seq_lens + b);
+    if (tl == 0 && h == 0 && lane == 0 && raw_len > a.len_cap && a.status) atomicOr(a.status, TQ_DEV_SEQ_TOO_LONG);
+    const int len = min(max(raw_len, 0), a.len_cap);
+    const int p0 = 16 * tl;
+    const uint8_t* tile = nullptr;
+    if (p0 < len) {
+      const int blk = ld_dep_s32(a.block_table + static_cast<long long>(b) * a.bt_stride + (p0 >> a.log2_bs));
+      if (blk < 0 || blk >= a.num_blocks) {
+        if (lane == 0 && a.status) atomicOr(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
+      } else {
+        tile = a.cache + ((static_cast<long long>(blk) * a.n_kv + h) * a.tiles_per_block + ((p0 & ((1 << a.log2_bs) - 1)) >> 4)) *
+                             static_cast<long long>(a.tile_bytes);
+      }
+    }
+    const int live = tile ? min(16, len - p0) : 0;   // rows 0 .. live - 1 hold cached positions
+
+    // ---- keys: C . H_R on tensor cores, then H_S across the 8 S-blocks
+    float d[8][2][4];
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) d[s2][nt][0] = d[s2][nt][1] = d[s2][nt][2] = d[s2][nt][3] = 0.f;
+    float ng = 0.f, nh = 0.f;
+    if (live > 0) {
+      uint4 kg, kh;
+      const uint8_t* kr = tile + a.k_off;
+      if constexpr (KMODE == kMse4) {
+        kg = ld_dep_u32x4(kr + g * a.k_row + 16 * t);
+        kh = ld_dep_u32x4(kr + (g + 8) * a.k_row + 16 * t);
+      } else {
+        const uint8_t* ra = kr + g * a.k_row + 12 * t;
+        const uint8_t* rb = kr + (g + 8) * a.k_row + 12 * t;
+        kg = make_uint4(ld_dep_u32(ra), ld_dep_u32(ra + 4), ld_dep_u32(ra + 8), 0u);
+        kh = make_uint4(ld_dep_u32(rb), ld_dep_u32(rb + 4), ld_dep_u32(rb + 8), 0u);
+      }
+      if (g < live) ng = half_bits(tile + a.knorm_off + 2 * g);
+      if (g + 8 < live) nh = half_bits(tile + a.knorm_off + 2 * (g + 8));
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2) {
+        const uint2 eg0 = lut[key_entry<KMODE>(kg, 2 * s2) * 32 + lane];
+        const uint2 eh0 = lut[key_entry<KMODE>(kh, 2 * s2) * 32 + lane];
+        const uint2 eg1 = lut[key_entry<KMODE>(kg, 2 * s2 + 1) * 32 + lane];
+        const uint2 eh1 = lut[key_entry<KMODE>(kh, 2 * s2 + 1) * 32 + lane];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          mma16816(d[s2][nt], eg0.x, eh0.x, eg1.x, eh1.x, hb[nt][0], hb[nt][1]);
+          mma16816(d[s2][nt], eg0.y, eh0.y, eg1.y, eh1.y, hb[nt][0], hb[nt][1]);
+        }
+      }
+    }
+    // H_S: Sylvester butterfly over the S-block index
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+      for (int s2 = 0; s2 < 8; ++s2) {
+        if (s2 & m) continue;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = d[s2][nt][e], x1 = d[s2 + m][nt][e];
+            d[s2][nt][e] = x0 + x1;
+            d[s2 + m][nt][e] = x0 - x1;
+          }
+      }
+    // stored_norm / sqrt(128) (zero for rows without a cached position), staged row-major
+    const float fg = ng * 0.088388347648318440f, fh = nh * 0.088388347648318440f;
+    __syncwarp();   // the previous tile's staged rows have been read
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int col = 2 * (t & 1) + 32 * (t >> 1) + 64 * nt + 4 * s2;   // coordinates col, col + 1
+        uint8_t* rg = stage + g * kRow + col * static_cast<int>(sizeof(T));
+        uint8_t* rh = stage + (g + 8) * kRow + col * static_cast<int>(sizeof(T));
+        if constexpr (std::is_same<T, float>::value) {
+          *reinterpret_cast<float2*>(rg) = make_float2(d[s2][nt][0] * fg, d[s2][nt][1] * fg);
+          *reinterpret_cast<float2*>(rh) = make_float2(d[s2][nt][2] * fh, d[s2][nt][3] * fh);
+        } else {
+          *reinterpret_cast<uint32_t*>(rg) = pack2<T>(d[s2][nt][0] * fg, d[s2][nt][1] * fg);
+          *reinterpret_cast<uint32_t*>(rh) = pack2<T>(d[s2][nt][2] * fh, d[s2][nt][3] * fh);
+        }
+      }
+    __syncwarp();
+    // whole rows out: 16 rows x 128 coordinates, 16 bytes a lane
+    constexpr int kChunks = kD * static_cast<int>(sizeof(T)) / 16;   // 16-byte chunks per row
+#pragma unroll
+    for (int i = 0; i < 16 * kChunks / 32; ++i) {
+      const int c = i * 32 + lane, r = c / kChunks, k = c - r * kChunks;
+      const int p = p0 + r;
+      if (p < a.max_seq_len) {
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * kRow + 16 * k);
+        *reinterpret_cast<uint4*>(static_cast<T*>(a.key_out) +
+                                  ((static_cast<long long>(b) * a.max_seq_len + p) * a.n_kv + h) * kD + k * 16 / sizeof(T)) = v;
+      }
+    }
+
+    // ---- values: lane (pair lane >> 2, q = lane & 3) expands coordinates 8 q + 32 k of both tokens
+    const int pair = lane >> 2, q = lane & 3;
+    float sv[2] = {0.f, 0.f}, zv[2] = {0.f, 0.f};
+    uint2 vw[4] = {};
+    if (live > 0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) vw[k] = value_pair_words<VBITS>(tile, a, pair, q + 4 * k);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (2 * pair + j < live) {
+          sv[j] = half_bits(tile + a.vscale_off + 2 * (2 * pair + j));
+          zv[j] = half_bits(tile + a.vzero_off + 2 * (2 * pair + j));
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int p = p0 + 2 * pair + j;
+      const bool row_live = 2 * pair + j < live;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t codes = token_codes<VBITS>(vw[k], j, q + 4 * k);
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          v[i] = row_live ? fmaf(sv[j], static_cast<float>((codes >> (VBITS * i)) & ((1u << VBITS) - 1)), zv[j]) : 0.f;
+        if (p < a.max_seq_len)
+          store8<T>(a.value_out, ((static_cast<long long>(b) * a.max_seq_len + p) * a.n_kv + h) * kD + 8 * (q + 4 * k), v);
+      }
+    }
+  }
+}
+
+template <int KMODE, int VBITS, typename T>
+cudaError_t launch_dequant_mma(const DequantArgs& a, int batch, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(lut_entries<KMODE>()) * 32 * 8 +
+                      static_cast<size_t>(kMmaWarps) * 16 * (kD * sizeof(T) + 16);
+  auto k = dequant_mma_kernel<KMODE, VBITS, T>;
+  cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+  const long long total = static_cast<long long>(a.seq_tiles) * batch * a.n_kv;
+  const long long want = (total + kMmaWarps - 1) / kMmaWarps;
+  (void)batch;
+  return launch_pdl(k, dim3(static_cast<unsigned>(want < sms ? want : sms)), dim3(kMmaWarps * 32), smem, stream, a);
+}
+
 template <int KMODE, int VBITS>
 cudaError_t launch_dequant(const DequantArgs& a, int batch, int out_dtype, cudaStream_t stream) {
+  if constexpr (KMODE != kFp8) {   // index-coded keys: the tensor-core form
+    if (out_dtype == TQ_DTYPE_BF16) return launch_dequant_mma<KMODE, VBITS, __nv_bfloat16>(a, batch, stream);
+    if (out_dtype == TQ_DTYPE_F16) return launch_dequant_mma<KMODE, VBITS, __half>(a, batch, stream);
+    return launch_dequant_mma<KMODE, VBITS, float>(a, batch, stream);
+  }
   const dim3 grid(static_cast<unsigned>(static_cast<long long>(a.seq_tiles) * batch), static_cast<unsigned>(a.n_kv));
   const dim3 block(kDequantWarps * 32);
   if (out_dtype == TQ_DTYPE_BF16)
@@ -250,6 +531,7 @@ extern "C" tq_status tq_dequant(const tq_config* cfg, const tq_codebook* cb,
   if (dev_status && (reinterpret_cast<unsigned long long>(dev_status) & 3ull)) return TQ_ERR_MISALIGNED;
   const long long seq_tiles = (static_cast<long long>(max_seq_len) + kTileTokens - 1) / kTileTokens;
   if (seq_tiles * batch > 0x7fffffffll || cfg->num_kv_heads > 65535) return TQ_ERR_INVALID_ARG;
+  if (seq_tiles * batch * cfg->num_kv_heads >= (1ll << 32)) return TQ_ERR_UNSUPPORTED;   // 32-bit tile index
 
   DequantArgs a;
   a.cache = static_cast<const uint8_t*>(cache);
@@ -261,6 +543,7 @@ extern "C" tq_status tq_dequant(const tq_config* cfg, const tq_codebook* cb,
   a.num_blocks = num_blocks;
   a.n_kv = cfg->num_kv_heads;
   a.max_seq_len = max_seq_len;
+  a.batch = batch;
   a.seq_tiles = static_cast<int>(seq_tiles);
   const long long cap = static_cast<long long>(bt_stride) * cfg->block_size;
   a.len_cap = static_cast<int>(cap < max_seq_len ? cap : max_seq_len);

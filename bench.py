@@ -691,7 +691,7 @@ def run_dequant(args):
         "ms_per_step": ms, "higher_is_better": True, "dtype": "f32 arithmetic, bf16 out", "data": "synthetic",
         "config": {"workload": _workload_text(w, ", bf16 out"),
                    "l2": "each launch moves %.0f MB (> L2)" % (nbytes / 1e6), "bytes_per_launch": nbytes},
-        "roofline": {"kernel": "dequant_kernel (tq_dequant)", "bound": "hbm", "achieved": gbs, "peak": peak,
+        "roofline": {"kernel": "dequant_mma_kernel (tq_dequant)", "bound": "hbm", "achieved": gbs, "peak": peak,
                      "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src, "ms_per_launch": ms,
                      "traffic": _profile_field("tq_dequant.cu", "dequant_gqa.md", "dram_bytes_per_launch"),
                      "algorithmic_bytes_per_launch": nbytes},

@@ -237,7 +237,6 @@ dequant_kernel(const DequantArgs a) {
 // and written back as full rows. Values are expanded in the same pass with a
 // row-major lane map (lane: token pair lane >> 2, coordinates 8 (lane & 3) +
 // 32 k), so their 16-byte stores cover whole sectors.
-constexpr int kMmaWarps = 16;
 
 template <int KMODE>
 __host__ __device__ constexpr int lut_entries() { return KMODE == kMse4 ? 256 : 64; }
@@ -274,20 +273,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   }
 }
 
-// The 8-byte value words of token pair `pair` that hold, for both tokens,
-// the codes of coordinates 8 l .. 8 l + 7 (as the row-major kernel reads them).
-template <int VBITS>
-__device__ __forceinline__ uint2 value_pair_words(const uint8_t* tile, const DequantArgs& a, int pair, int l) {
-  if constexpr (VBITS == 4) {
-    const int swz = (a.v_row % 64 == 0) ? 2 * (pair & 3) : 0;
-    return ld_dep_u32x2(tile + a.v_off + pair * 2 * a.v_row + 16 * ((l >> 1) ^ swz) + 8 * (l & 1));
-  } else {
-    const int w0 = 3 * (l >> 1) + (l & 1);
-    const uint8_t* pw = tile + a.v_off + pair * 2 * a.v_row + 4 * w0;
-    return make_uint2(ld_dep_u32(pw), ld_dep_u32(pw + 4));
-  }
-}
-
 // Codes of coordinates 8 l .. 8 l + 7 of token j (0, 1) of the pair, LSB first.
 template <int VBITS>
 __device__ __forceinline__ uint32_t token_codes(uint2 vw, int j, int l) {
@@ -299,15 +284,84 @@ __device__ __forceinline__ uint32_t token_codes(uint2 vw, int j, int l) {
   }
 }
 
+template <typename T>
+__host__ __device__ constexpr int dq_warps() { return sizeof(T) == 4 ? 8 : 16; }   // shared memory per CTA
+constexpr int kMaxTileBytes = 2144;   // largest index-coded-key tile (4bit_nc)
+
+// The 8-byte value words of token pair `pair` (tile in shared memory) that
+// hold, for both tokens, the codes of coordinates 8 l .. 8 l + 7.
+template <int VBITS>
+__device__ __forceinline__ uint2 value_pair_words_s(const uint8_t* tile, const DequantArgs& a, int pair, int l) {
+  if constexpr (VBITS == 4) {
+    const int swz = (a.v_row % 64 == 0) ? 2 * (pair & 3) : 0;
+    return *reinterpret_cast<const uint2*>(tile + a.v_off + pair * 2 * a.v_row + 16 * ((l >> 1) ^ swz) + 8 * (l & 1));
+  } else {
+    const int w0 = 3 * (l >> 1) + (l & 1);
+    const uint32_t* pw = reinterpret_cast<const uint32_t*>(tile + a.v_off + pair * 2 * a.v_row + 4 * w0);
+    return make_uint2(pw[0], pw[1]);
+  }
+}
+
+// Where tile u of the (sequence, tile, KV head) order lives. The length and
+// block id are loaded here and used a tile later, so the loads overlap work.
+struct DqTile {
+  int b, tl, h, raw_len, blk;   // blk: -2 when no entry is read
+};
+
+__device__ __forceinline__ DqTile dq_resolve(const DequantArgs& a, unsigned u, unsigned total) {
+  DqTile r{0, 0, 0, 0, -2};
+  if (u < total) {
+    const unsigned bt = u / static_cast<unsigned>(a.n_kv);
+    r.h = static_cast<int>(u - bt * static_cast<unsigned>(a.n_kv));
+    r.b = static_cast<int>(bt / static_cast<unsigned>(a.seq_tiles));
+    r.tl = static_cast<int>(bt - static_cast<unsigned>(r.b) * static_cast<unsigned>(a.seq_tiles));
+    r.raw_len = ld_dep_s32(a.seq_lens + r.b);
+    if (16 * r.tl < a.len_cap)
+      r.blk = ld_dep_s32(a.block_table + static_cast<long long>(r.b) * a.bt_stride + ((16 * r.tl) >> a.log2_bs));
+  }
+  return r;
+}
+
+// The tile's address (null when it holds no cached position) and its number of
+// cached rows; flags a bad block id or an over-long length (lane 0).
+__device__ __forceinline__ const uint8_t* dq_address(const DequantArgs& a, const DqTile& r, int lane, int* live) {
+  const int len = min(max(r.raw_len, 0), a.len_cap);
+  if (lane == 0 && r.tl == 0 && r.h == 0 && r.raw_len > a.len_cap && a.status) atomicOr(a.status, TQ_DEV_SEQ_TOO_LONG);
+  *live = 0;
+  if (16 * r.tl >= len) return nullptr;
+  if (r.blk < 0 || r.blk >= a.num_blocks) {
+    if (lane == 0 && a.status) atomicOr(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
+    return nullptr;
+  }
+  *live = min(16, len - 16 * r.tl);
+  return a.cache + ((static_cast<long long>(r.blk) * a.n_kv + r.h) * a.tiles_per_block +
+                    (((16 * r.tl) & ((1 << a.log2_bs) - 1)) >> 4)) * static_cast<long long>(a.tile_bytes);
+}
+
+__device__ __forceinline__ void dq_copy(uint8_t* slot, const uint8_t* src, int chunks, int lane) {
+  if (src) {
+    for (int c = lane; c < chunks; c += 32) {
+      const unsigned d = static_cast<unsigned>(__cvta_generic_to_shared(slot + 16 * c));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src + 16 * c) : "memory");
+    }
+  }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+// Persistent: warp w of CTA c takes tiles c * warps + w, + all warps, ...; each
+// tile's bytes arrive by cp.async in one of two per-warp slots while the
+// previous tile is computed.
 template <int KMODE, int VBITS, typename T>
-__global__ void __launch_bounds__(kMmaWarps * 32, 1) dequant_mma_kernel(const DequantArgs a) {
+__global__ void __launch_bounds__(dq_warps<T>() * 32, 1) dequant_mma_kernel(const DequantArgs a) {
   extern __shared__ __align__(16) uint8_t s_dq[];
+  constexpr int kWarpsT = dq_warps<T>();
   constexpr int kRow = kD * static_cast<int>(sizeof(T)) + 16;   // staging row stride (bytes)
   uint2* lut = reinterpret_cast<uint2*>(s_dq);                   // [entry][lane]: (hi, lo) half2 pair
   grid_dep_wait();   // cache, tables and lengths may come from the previous kernel
   grid_dep_launch();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, t = lane & 3;
-  uint8_t* stage = s_dq + lut_entries<KMODE>() * 32 * 8 + warp * 16 * kRow;
+  uint8_t* stage = s_dq + lut_entries<KMODE>() * 32 * 8 + warp * (16 * kRow + 2 * kMaxTileBytes);
+  uint8_t* slots = stage + 16 * kRow;
   constexpr int kShift = KMODE == kMse4 ? 4 : 3;
   for (int i = tid; i < lut_entries<KMODE>() * 32; i += blockDim.x) {
     const int e = i >> 5;
@@ -338,27 +392,24 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) dequant_mma_kernel(const De
 
   // tiles in (sequence, tile, KV head) order, so neighbouring warps write neighbouring output rows
   const unsigned total = static_cast<unsigned>(a.seq_tiles) * static_cast<unsigned>(a.batch) * static_cast<unsigned>(a.n_kv);
-  const unsigned nwarps = gridDim.x * kMmaWarps;
-  for (unsigned u = blockIdx.x * kMmaWarps + warp; u < total; u += nwarps) {
-    const unsigned bt = u / static_cast<unsigned>(a.n_kv);
-    const int h = static_cast<int>(u - bt * static_cast<unsigned>(a.n_kv));
-    const int b = static_cast<int>(bt / static_cast<unsigned>(a.seq_tiles));
-    const int tl = static_cast<int>(bt - static_cast<unsigned>(b) * static_cast<unsigned>(a.seq_tiles));
-    const int raw_len = ld_dep_s32(a.seq_lens + b);
-    if (tl == 0 && h == 0 && lane == 0 && raw_len > a.len_cap && a.status) atomicOr(a.status, TQ_DEV_SEQ_TOO_LONG);
-    const int len = min(max(raw_len, 0), a.len_cap);
-    const int p0 = 16 * tl;
-    const uint8_t* tile = nullptr;
-    if (p0 < len) {
-      const int blk = ld_dep_s32(a.block_table + static_cast<long long>(b) * a.bt_stride + (p0 >> a.log2_bs));
-      if (blk < 0 || blk >= a.num_blocks) {
-        if (lane == 0 && a.status) atomicOr(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
-      } else {
-        tile = a.cache + ((static_cast<long long>(blk) * a.n_kv + h) * a.tiles_per_block + ((p0 & ((1 << a.log2_bs) - 1)) >> 4)) *
-                             static_cast<long long>(a.tile_bytes);
-      }
-    }
-    const int live = tile ? min(16, len - p0) : 0;   // rows 0 .. live - 1 hold cached positions
+  const unsigned nwarps = gridDim.x * kWarpsT;
+  const int chunks = a.tile_bytes >> 4;
+  unsigned u = blockIdx.x * kWarpsT + warp;
+  DqTile cur = dq_resolve(a, u, total);
+  int cur_live = 0;
+  const uint8_t* cur_src = dq_address(a, cur, lane, &cur_live);
+  dq_copy(slots, cur_src, chunks, lane);
+  DqTile nxt = dq_resolve(a, u + nwarps, total);
+  for (int i = 0; u < total; ++i, u += nwarps) {
+    // next tile's copies, the one after's indices
+    int nxt_live = 0;
+    const uint8_t* nxt_src = u + nwarps < total ? dq_address(a, nxt, lane, &nxt_live) : nullptr;
+    dq_copy(slots + ((i + 1) & 1) * kMaxTileBytes, nxt_src, chunks, lane);
+    const DqTile nn = dq_resolve(a, u + 2 * nwarps, total);
+    asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // this lane's copies of tile i
+    __syncwarp();                                              // and every lane's
+    const uint8_t* tile = slots + (i & 1) * kMaxTileBytes;
+    const int live = cur_live, b = cur.b, h = cur.h, p0 = 16 * cur.tl;
 
     // ---- keys: C . H_R on tensor cores, then H_S across the 8 S-blocks
     float d[8][2][4];
@@ -371,16 +422,16 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) dequant_mma_kernel(const De
       uint4 kg, kh;
       const uint8_t* kr = tile + a.k_off;
       if constexpr (KMODE == kMse4) {
-        kg = ld_dep_u32x4(kr + g * a.k_row + 16 * t);
-        kh = ld_dep_u32x4(kr + (g + 8) * a.k_row + 16 * t);
+        kg = *reinterpret_cast<const uint4*>(kr + g * a.k_row + 16 * t);
+        kh = *reinterpret_cast<const uint4*>(kr + (g + 8) * a.k_row + 16 * t);
       } else {
-        const uint8_t* ra = kr + g * a.k_row + 12 * t;
-        const uint8_t* rb = kr + (g + 8) * a.k_row + 12 * t;
-        kg = make_uint4(ld_dep_u32(ra), ld_dep_u32(ra + 4), ld_dep_u32(ra + 8), 0u);
-        kh = make_uint4(ld_dep_u32(rb), ld_dep_u32(rb + 4), ld_dep_u32(rb + 8), 0u);
+        const uint32_t* ra = reinterpret_cast<const uint32_t*>(kr + g * a.k_row + 12 * t);
+        const uint32_t* rb = reinterpret_cast<const uint32_t*>(kr + (g + 8) * a.k_row + 12 * t);
+        kg = make_uint4(ra[0], ra[1], ra[2], 0u);
+        kh = make_uint4(rb[0], rb[1], rb[2], 0u);
       }
-      if (g < live) ng = half_bits(tile + a.knorm_off + 2 * g);
-      if (g + 8 < live) nh = half_bits(tile + a.knorm_off + 2 * (g + 8));
+      if (g < live) ng = __half2float(*reinterpret_cast<const __half*>(tile + a.knorm_off + 2 * g));
+      if (g + 8 < live) nh = __half2float(*reinterpret_cast<const __half*>(tile + a.knorm_off + 2 * (g + 8)));
 #pragma unroll
       for (int s2 = 0; s2 < 8; ++s2) {
         const uint2 eg0 = lut[key_entry<KMODE>(kg, 2 * s2) * 32 + lane];
@@ -411,7 +462,6 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) dequant_mma_kernel(const De
       }
     // stored_norm / sqrt(128) (zero for rows without a cached position), staged row-major
     const float fg = ng * 0.088388347648318440f, fh = nh * 0.088388347648318440f;
-    __syncwarp();   // the previous tile's staged rows have been read
 #pragma unroll
     for (int s2 = 0; s2 < 8; ++s2)
 #pragma unroll
@@ -427,19 +477,6 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) dequant_mma_kernel(const De
           *reinterpret_cast<uint32_t*>(rh) = pack2<T>(d[s2][nt][2] * fh, d[s2][nt][3] * fh);
         }
       }
-    __syncwarp();
-    // whole rows out: 16 rows x 128 coordinates, 16 bytes a lane
-    constexpr int kChunks = kD * static_cast<int>(sizeof(T)) / 16;   // 16-byte chunks per row
-#pragma unroll
-    for (int i = 0; i < 16 * kChunks / 32; ++i) {
-      const int c = i * 32 + lane, r = c / kChunks, k = c - r * kChunks;
-      const int p = p0 + r;
-      if (p < a.max_seq_len) {
-        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * kRow + 16 * k);
-        *reinterpret_cast<uint4*>(static_cast<T*>(a.key_out) +
-                                  ((static_cast<long long>(b) * a.max_seq_len + p) * a.n_kv + h) * kD + k * 16 / sizeof(T)) = v;
-      }
-    }
 
     // ---- values: lane (pair lane >> 2, q = lane & 3) expands coordinates 8 q + 32 k of both tokens
     const int pair = lane >> 2, q = lane & 3;
@@ -447,13 +484,26 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) dequant_mma_kernel(const De
     uint2 vw[4] = {};
     if (live > 0) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) vw[k] = value_pair_words<VBITS>(tile, a, pair, q + 4 * k);
+      for (int k = 0; k < 4; ++k) vw[k] = value_pair_words_s<VBITS>(tile, a, pair, q + 4 * k);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         if (2 * pair + j < live) {
-          sv[j] = half_bits(tile + a.vscale_off + 2 * (2 * pair + j));
-          zv[j] = half_bits(tile + a.vzero_off + 2 * (2 * pair + j));
+          sv[j] = __half2float(*reinterpret_cast<const __half*>(tile + a.vscale_off + 2 * (2 * pair + j)));
+          zv[j] = __half2float(*reinterpret_cast<const __half*>(tile + a.vzero_off + 2 * (2 * pair + j)));
         }
+      }
+    }
+    __syncwarp();   // staged key rows complete; every lane has read the slot
+    // whole key rows out: 16 rows x 128 coordinates, 16 bytes a lane
+    constexpr int kChunks = kD * static_cast<int>(sizeof(T)) / 16;   // 16-byte chunks per row
+#pragma unroll
+    for (int i2 = 0; i2 < 16 * kChunks / 32; ++i2) {
+      const int c = i2 * 32 + lane, r = c / kChunks, k = c - r * kChunks;
+      const int p = p0 + r;
+      if (p < a.max_seq_len) {
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * kRow + 16 * k);
+        *reinterpret_cast<uint4*>(static_cast<T*>(a.key_out) +
+                                  ((static_cast<long long>(b) * a.max_seq_len + p) * a.n_kv + h) * kD + k * 16 / sizeof(T)) = v;
       }
     }
 #pragma unroll
@@ -465,19 +515,25 @@ __global__ void __launch_bounds__(kMmaWarps * 32, 1) dequant_mma_kernel(const De
         const uint32_t codes = token_codes<VBITS>(vw[k], j, q + 4 * k);
         float v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          v[i] = row_live ? fmaf(sv[j], static_cast<float>((codes >> (VBITS * i)) & ((1u << VBITS) - 1)), zv[j]) : 0.f;
+        for (int i3 = 0; i3 < 8; ++i3)
+          v[i3] = row_live ? fmaf(sv[j], static_cast<float>((codes >> (VBITS * i3)) & ((1u << VBITS) - 1)), zv[j]) : 0.f;
         if (p < a.max_seq_len)
           store8<T>(a.value_out, ((static_cast<long long>(b) * a.max_seq_len + p) * a.n_kv + h) * kD + 8 * (q + 4 * k), v);
       }
     }
+    __syncwarp();   // the staged rows have been read before the next tile writes them
+    cur = nxt;
+    cur_live = nxt_live;
+    nxt = nn;
   }
+  asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy outlives the CTA
 }
 
 template <int KMODE, int VBITS, typename T>
 cudaError_t launch_dequant_mma(const DequantArgs& a, int batch, cudaStream_t stream) {
+  if (a.tile_bytes > kMaxTileBytes) return cudaErrorInvalidValue;
   const size_t smem = static_cast<size_t>(lut_entries<KMODE>()) * 32 * 8 +
-                      static_cast<size_t>(kMmaWarps) * 16 * (kD * sizeof(T) + 16);
+                      static_cast<size_t>(dq_warps<T>()) * (16 * (kD * sizeof(T) + 16) + 2 * kMaxTileBytes);
   auto k = dequant_mma_kernel<KMODE, VBITS, T>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (err != cudaSuccess) return err;
@@ -485,9 +541,8 @@ cudaError_t launch_dequant_mma(const DequantArgs& a, int batch, cudaStream_t str
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
   const long long total = static_cast<long long>(a.seq_tiles) * batch * a.n_kv;
-  const long long want = (total + kMmaWarps - 1) / kMmaWarps;
-  (void)batch;
-  return launch_pdl(k, dim3(static_cast<unsigned>(want < sms ? want : sms)), dim3(kMmaWarps * 32), smem, stream, a);
+  const long long want = (total + dq_warps<T>() - 1) / dq_warps<T>();
+  return launch_pdl(k, dim3(static_cast<unsigned>(want < sms ? want : sms)), dim3(dq_warps<T>() * 32), smem, stream, a);
 }
 
 template <int KMODE, int VBITS>

@@ -118,17 +118,29 @@ store_kernel(const StoreArgs a) {
   const int l = lane & 15;
   const long long vec = static_cast<long long>(blockIdx.x) * kVecsPerCta + (threadIdx.x >> 4);
   bool live = vec < a.num_vectors;
-  long long tok = 0;
+  long long tok = 0, slot = -1;
   int head = 0;
-  uint8_t* tile = nullptr;
-  int r = 0;
   if (live) {
     // vec / n_kv by multiply and shift whenever the vector count allows
     tok = a.num_vectors < (1ll << 31)
               ? static_cast<long long>(__umulhi(2u * static_cast<unsigned>(vec), a.kv_magic) >> a.kv_shift)
               : vec / a.n_kv;
     head = static_cast<int>(vec - tok * a.n_kv);
-    const long long slot = ld_dep_s64(a.slots + tok);
+    slot = ld_dep_s64(a.slots + tok);
+  }
+  // the inputs' addresses do not depend on the slot: their loads go out with
+  // the slot's, not after it
+  float k[8], v[8];
+  if (live) {
+    load8<T>(a.key, vec * kD + 8 * l, k);
+    load8<T>(a.value, vec * kD + 8 * l, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) k[j] = v[j] = 0.f;
+  }
+  uint8_t* tile = nullptr;
+  int r = 0;
+  if (live) {
     const long long blk = slot >> a.log2_bs;
     if (slot < 0) {
       live = false;
@@ -140,15 +152,6 @@ store_kernel(const StoreArgs a) {
       tile = a.cache + ((blk * a.n_kv + head) * a.tiles_per_block + (off >> 4)) * static_cast<long long>(a.tile_bytes);
       r = off & 15;
     }
-  }
-
-  float k[8], v[8];
-  if (live) {
-    load8<T>(a.key, vec * kD + 8 * l, k);
-    load8<T>(a.value, vec * kD + 8 * l, v);
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) k[j] = v[j] = 0.f;
   }
 
   // ---------------- keys ----------------

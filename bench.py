@@ -790,7 +790,7 @@ for _ in range({steps}):
 print(json.dumps({{"times": times}}))
 """
 PROD_ORACLE_TOKENS = 4096
-FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12   # SMs x fp32 lanes x FMA x max SM clock
+TF32_PER_BF16 = 1.1 / 2.25   # nominal dense tf32 / bf16 tensor rates of the part
 
 
 def run_prod(args):
@@ -799,8 +799,9 @@ def run_prod(args):
     each step is tq_prod_scores of every query head against every cached key
     (a query-prep launch and the scores launch); four copies of the 54.5 MB
     cache are rotated so no step finds its keys in L2. The line also carries
-    tq_prod_store of an 8192-token bf16 prefill chunk (bound by the fp32
-    projection S r) and the oracle's prod_scores on one whole sequence
+    tq_prod_store of an 8192-token bf16 prefill chunk (its contraction, the
+    projection S r, runs on TF32 tensor cores) and the oracle's prod_scores
+    on one whole sequence
     (4096 positions). Prints one JSON line of its own."""
     import torch
 
@@ -858,6 +859,8 @@ def run_prod(args):
     peak, peak_src = _peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
     store_tflops = STORE_TOKENS * w.n_kv * 2 * w.d * w.d / (ms_store * 1e-3) / 1e12
+    tpeak, tpeak_src = _tensor_peak()
+    tf32_peak = tpeak * TF32_PER_BF16
     line = {
         "op": "prod", "metric": "TurboQuant_prod scores GB/s (packed prod keys read + fp32 scores written); keys/s",
         "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": reps, "warmup": args.warmup, "ms_per_step": ms,
@@ -872,10 +875,12 @@ def run_prod(args):
                      "traffic": _profile_field("tq_prod.cu", "prod_scores_prod.md", "dram_bytes_per_launch")},
         "store": {"kernel": "prod_store_kernel (tq_prod_store)", "tokens": STORE_TOKENS,
                   "mtok_s": STORE_TOKENS / (ms_store * 1e-3) / 1e6, "ms_per_launch": ms_store,
-                  "roofline": {"bound": "alu", "achieved": store_tflops, "peak": FP32_PEAK_TFLOPS,
-                               "unit": "TFLOP/s", "frac": store_tflops / FP32_PEAK_TFLOPS,
-                               "peak_source": "derived: 152 SMs x 128 fp32 FMA/clk x 2 x 2070 MHz",
-                               "flops_per_launch": STORE_TOKENS * w.n_kv * 2 * w.d * w.d}},
+                  "roofline": {"bound": "tensor", "achieved": store_tflops, "peak": tf32_peak,
+                               "unit": "TFLOP/s", "frac": store_tflops / tf32_peak,
+                               "peak_source": tpeak_src + " x %.3f (nominal tf32 / bf16 dense ratio)" % TF32_PER_BF16,
+                               "flops_per_launch": STORE_TOKENS * w.n_kv * 2 * w.d * w.d,
+                               "traffic": _profile_field("tq_prod_store.cu", "prod_store_prod.md",
+                                                         "dram_bytes_per_launch")}},
         "gpu_launches": 2 * reps + 20,
         "clocks": clk.summary(),
     }

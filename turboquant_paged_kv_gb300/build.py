@@ -29,7 +29,7 @@ NVCC_FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
 CU_SOURCES = ["tq_store.cu", "tq_decode.cu", "tq_decode_noalloc.cu", "tq_dequant.cu", "tq_prod.cu",
-              "tq_continue.cu"]
+              "tq_prod_store.cu", "tq_continue.cu"]
 CPP_SOURCES = ["tq_host.cpp"]
 
 
@@ -40,6 +40,7 @@ def _sources():
 def _deps():
     return _sources() + [os.path.join(CSRC, "tq_internal.h"), os.path.join(CSRC, "tq_launch.cuh"),
                          os.path.join(CSRC, "tq_vec.cuh"), os.path.join(CSRC, "tq_attn.cuh"),
+                         os.path.join(CSRC, "tq_prod.cuh"),
                          os.path.join(INCLUDE, "tq.h"),
                          os.path.abspath(__file__)]
 

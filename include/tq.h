@@ -215,6 +215,38 @@ tq_status tq_decode(const tq_config* cfg, const tq_codebook* cb,
                     void* workspace, size_t workspace_bytes,
                     unsigned int* dev_status, tq_stream_t stream);
 
+/* Device. One decode step with its new tokens: stores each sequence's newest
+ * token into the cache, then returns what tq_decode returns over all
+ * seq_lens[b] positions, the new one included. The pages run the step as a
+ * cache write ([vLLM-TQ] "写入内核:store 路径如何旋转、量化与打包") followed by
+ * the decode ([vLLM-TQ] "读取内核"); here both happen in the decode's split
+ * kernel: the warp that reads the tile holding position seq_lens[b] - 1
+ * quantises that token's key and value with the store's arithmetic, writes
+ * them into the cache and uses them at once, so the step needs no separate
+ * store launch.
+ *   new_k, new_v  device [batch][n_kv][d], q_dtype, 16-byte aligned: the key
+ *                 and value of position seq_lens[b] - 1 of sequence b
+ *   cache         device, writable; row seq_lens[b] - 1 of each sequence ends
+ *                 up holding exactly the bytes tq_store writes for that token
+ *                 at slot block_table[b][p / block_size] * block_size +
+ *                 p % block_size, p = seq_lens[b] - 1
+ *   every other argument, layout and rule as for tq_decode (the workspace
+ *   size is tq_decode_workspace_size's).
+ * Not stored: sequences with seq_lens[b] == 0; sequences longer than
+ * max_seq_len or bt_stride * block_size (TQ_DEV_SEQ_TOO_LONG, cut as in
+ * tq_decode); a newest position whose block id is outside [0, num_blocks)
+ * (TQ_DEV_BLOCK_OUT_OF_RANGE). Launches the split kernel then the reduce
+ * kernel, like tq_decode. */
+tq_status tq_decode_append(const tq_config* cfg, const tq_codebook* cb,
+                           const void* q, int q_dtype,
+                           const void* new_k, const void* new_v,
+                           void* cache, long long num_blocks,
+                           const int* block_table, int bt_stride,
+                           const int* seq_lens, int batch, int max_seq_len, float scale,
+                           void* out, int out_dtype,
+                           void* workspace, size_t workspace_bytes,
+                           unsigned int* dev_status, tq_stream_t stream);
+
 /* The two stages of tq_decode, separately (same arguments and rules), for
  * callers that time or overlap them. tq_decode_partials writes only the
  * workspace; tq_decode_reduce reads it and writes out. */
@@ -432,8 +464,8 @@ const char* tq_status_string(int status);
 /* Host. ABI version of this header (major * 100 + minor). */
 int tq_version(void);
 
-#define TQ_ABI_VERSION 104   /* 1.01: tq_dequant; 1.02: 3bit_nc runs; 1.03: TurboQuant_prod (tq_prod_*);
-                                 1.04: tq_continue */
+#define TQ_ABI_VERSION 105   /* 1.01: tq_dequant; 1.02: 3bit_nc runs; 1.03: TurboQuant_prod (tq_prod_*);
+                                 1.04: tq_continue; 1.05: tq_decode_append */
 
 #ifdef __cplusplus
 }

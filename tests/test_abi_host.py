@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(tq):
     assert sorted(_abi.EXPORTED) == declared
     # matches the header's TQ_ABI_VERSION
     text = open(os.path.join(ROOT, "include", "tq.h")).read()
-    assert tq.tq_version() == int(re.search(r"#define TQ_ABI_VERSION (\d+)", text).group(1)) == 104
+    assert tq.tq_version() == int(re.search(r"#define TQ_ABI_VERSION (\d+)", text).group(1)) == 105
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
@@ -127,6 +127,31 @@ def test_host_argument_errors_return_before_launch(tq):
     assert dec(uneven, 1 << 30) == _abi.TQ_ERR_INVALID_ARG
     badpart = tq.make_config("4bit_nc", 32, 8, partition_tokens=40)
     assert dec(badpart, 1 << 30) == _abi.TQ_ERR_INVALID_ARG
+
+
+def test_decode_append_argument_errors_return_before_launch(tq):
+    from turboquant_paged_kv_gb300 import _abi
+    lib = _abi.load()
+    cfg = tq.make_config("4bit_nc", 32, 8)
+    cb = tq.tq_build_codebook(128, 4)
+    ok16 = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10008)
+    need = tq.tq_decode_workspace_size(cfg, 2, 64)
+
+    def app(new_k=ok16, new_v=ok16, out=ok16, ws_bytes=need, batch=2, out_dtype=2):
+        return lib.tq_decode_append(ctypes.byref(cfg), ctypes.byref(cb), ok16, 1, new_k, new_v, ok16, 10, ok16, 4,
+                                    ok16, batch, 64, 0.0, out, out_dtype, ok16, ws_bytes, None, None)
+
+    assert app(new_k=None) == _abi.TQ_ERR_INVALID_ARG
+    assert app(new_v=None) == _abi.TQ_ERR_INVALID_ARG
+    assert app(out=None) == _abi.TQ_ERR_INVALID_ARG
+    assert app(new_k=odd) == _abi.TQ_ERR_MISALIGNED
+    assert app(new_v=odd) == _abi.TQ_ERR_MISALIGNED
+    assert app(out=odd) == _abi.TQ_ERR_MISALIGNED
+    assert app(ws_bytes=need - 1) == _abi.TQ_ERR_WORKSPACE_TOO_SMALL
+    assert app(out_dtype=9) == _abi.TQ_ERR_INVALID_ARG
+    # an empty batch is a no-op even with null rows
+    assert app(new_k=None, new_v=None, batch=0) == _abi.TQ_OK
 
 
 def test_dequant_argument_errors_return_before_launch(tq):

@@ -32,7 +32,7 @@ _LIB = _LazyLib()
 
 _DTYPES = {torch.float16: TQ_DTYPE_F16, torch.bfloat16: TQ_DTYPE_BF16, torch.float32: TQ_DTYPE_F32}
 
-__all__ = ["make_config", "tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode",
+__all__ = ["make_config", "tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode", "tq_decode_append",
            "tq_decode_partials", "tq_decode_reduce", "tq_decode_noalloc", "tq_decode_workspace_size",
            "tq_dequant", "tq_prod_layout_for", "tq_prod_store", "tq_prod_scores_workspace_size",
            "tq_prod_scores", "tq_continue_workspace_size", "tq_continue",
@@ -113,6 +113,26 @@ def tq_decode(cfg: tq_config, cb, q: torch.Tensor, cache: torch.Tensor, block_ta
         num_blocks = cache.numel() // lay.block_bytes
     _abi.check("tq_decode", _LIB.tq_decode(
         ctypes.byref(cfg), _cb(cb), _ptr(q), _DTYPES[q.dtype], _ptr(cache), num_blocks,
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, float(scale),
+        _ptr(out), _DTYPES[out.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream)))
+
+
+def tq_decode_append(cfg: tq_config, cb, q: torch.Tensor, new_k: torch.Tensor, new_v: torch.Tensor,
+                     cache: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                     out: torch.Tensor, workspace: torch.Tensor, scale: float = 0.0, num_blocks: int | None = None,
+                     dev_status: torch.Tensor | None = None, stream=None) -> None:
+    """One decode step with its new tokens: new_k, new_v [B, n_kv, d] (q's
+    dtype) are stored at position seq_lens[b] - 1 of each sequence, then the
+    decode runs over all seq_lens[b] positions (one split and one reduce
+    launch, no store launch)."""
+    lay = tq_layout_for(cfg)
+    if num_blocks is None:
+        num_blocks = cache.numel() // lay.block_bytes
+    if new_k.dtype != q.dtype or new_v.dtype != q.dtype:
+        raise ValueError("new_k and new_v must have q's dtype")
+    _abi.check("tq_decode_append", _LIB.tq_decode_append(
+        ctypes.byref(cfg), _cb(cb), _ptr(q), _DTYPES[q.dtype], _ptr(new_k), _ptr(new_v), _ptr(cache), num_blocks,
         _ptr(block_table), block_table.shape[1], _ptr(seq_lens), q.shape[0], max_seq_len, float(scale),
         _ptr(out), _DTYPES[out.dtype], _ptr(workspace), workspace.numel() * workspace.element_size(),
         _ptr(dev_status), _stream(stream)))

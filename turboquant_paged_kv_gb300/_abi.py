@@ -37,7 +37,7 @@ TQ_DEV_TIMEOUT = 8
 
 # every function tq.h declares (checked by the ABI tests)
 EXPORTED = ("tq_build_codebook", "tq_layout_for", "tq_store", "tq_decode_workspace_size",
-            "tq_decode", "tq_decode_partials", "tq_decode_reduce", "tq_decode_noalloc",
+            "tq_decode", "tq_decode_append", "tq_decode_partials", "tq_decode_reduce", "tq_decode_noalloc",
             "tq_dequant", "tq_prod_layout_for", "tq_prod_store", "tq_prod_scores_workspace_size",
             "tq_prod_scores", "tq_continue_workspace_size", "tq_continue", "tq_status_string", "tq_version")
 
@@ -87,6 +87,8 @@ _SIGS = {
     "tq_decode_workspace_size": (_sz, [ctypes.POINTER(tq_config), _i, _i]),
     "tq_decode": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_codebook), _vp, _i, _vp, _ll, _vp, _i,
                        _vp, _i, _i, _f, _vp, _i, _vp, _sz, _vp, _vp]),
+    "tq_decode_append": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_codebook), _vp, _i, _vp, _vp, _vp,
+                              _ll, _vp, _i, _vp, _i, _i, _f, _vp, _i, _vp, _sz, _vp, _vp]),
     "tq_decode_partials": (_i, [ctypes.POINTER(tq_config), ctypes.POINTER(tq_codebook), _vp, _i, _vp, _ll,
                                 _vp, _i, _vp, _i, _i, _f, _vp, _sz, _vp, _vp]),
     "tq_decode_reduce": (_i, [ctypes.POINTER(tq_config), _vp, _i, _i, _i, _vp, _i, _vp, _sz, _vp]),

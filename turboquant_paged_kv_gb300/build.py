@@ -40,7 +40,7 @@ def _sources():
 def _deps():
     return _sources() + [os.path.join(CSRC, "tq_internal.h"), os.path.join(CSRC, "tq_launch.cuh"),
                          os.path.join(CSRC, "tq_vec.cuh"), os.path.join(CSRC, "tq_attn.cuh"),
-                         os.path.join(CSRC, "tq_prod.cuh"),
+                         os.path.join(CSRC, "tq_prod.cuh"), os.path.join(CSRC, "tq_store.cuh"),
                          os.path.join(INCLUDE, "tq.h"),
                          os.path.abspath(__file__)]
 

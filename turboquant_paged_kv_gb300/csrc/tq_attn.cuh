@@ -41,11 +41,21 @@ struct DecodeArgs {
   int tile_bytes, k_off, v_off, knorm_off, vscale_off, vzero_off;
   int stage_bytes;     // ring stage: kChunk tiles, then the descriptor
   int desc_off;        // offset of the descriptor in a stage
-  int qbuf_bytes;      // G * d * 2
+  int qbuf_bytes;      // G * d * 2: the query rows of a segment
+  int qslot_bytes;     // a consumer's query slot: the query rows, then (append) the raw K and V rows
   int dyn_bytes;
   float qscale;        // softmax scale * log2(e)
   int early_indices;   // TQ_FLAG_INDICES_READY: lengths and block ids read before the dependency wait
   float cent[16];
+  // append (tq_decode_append; new_k null: off): each sequence's newest token,
+  // position seq_lens[b] - 1, is quantised and written into the cache by the
+  // consumer warp that reads its tile
+  const void* new_k;   // [batch][n_kv][d], the query's dtype
+  const void* new_v;
+  uint8_t* wcache;     // the cache, writable
+  int k_row, v_row;    // bytes per position of the key and value regions
+  float mid[15];       // key codebook midpoints and centroids (unscaled)
+  float scent[16];
 };
 
 struct ReduceArgs {

@@ -90,6 +90,7 @@
 #include <type_traits>
 
 #include "tq_attn.cuh"
+#include "tq_store.cuh"
 #include "tq_internal.h"
 #include "tq_launch.cuh"
 
@@ -126,10 +127,15 @@ static_assert(kMaxConsumers <= kRecordWarps, "workspace sized for at most 16 con
 static_assert(kMaxConsumers <= 32 * kProducers, "one producer lane per consumer warp");
 static_assert(kMaxConsumers + kProducers <= 12, "12 warps keep 168 registers per thread");
 // Shared-memory head: mbarriers (full and empty per (consumer, stage), then one
-// "q empty" per consumer) in the first kBarHead bytes, then one query slot of
+// "q empty" per consumer) from the start, the key codebook for the append
+// path (16 midpoints, 16 centroids) in the last 128 bytes of the first
+// kBarHead bytes, then one query slot of
 // G * d * 2 bytes per consumer.
 constexpr uint32_t kBarHead = 1024;
-static_assert((2 * kMaxConsumers * kStages + kMaxConsumers) * 8 <= static_cast<int>(kBarHead), "barrier area");
+constexpr uint32_t kCodebookOff = kBarHead - 128;
+static_assert((2 * kMaxConsumers * kStages + 2 * kMaxConsumers) * 8 <= static_cast<int>(kCodebookOff), "barrier area");
+constexpr uint32_t kAppendBit = 1024;   // descriptor: the stage carries the newest token's raw K and V rows
+constexpr uint32_t kRawRowBytes = kD * 2;
 static_assert(kStages >= 2 && kChunk >= 1 && kChunk <= 4, "ring shape");
 
 // ---------------------------------------------------------------- ring plan
@@ -176,6 +182,10 @@ __device__ __forceinline__ uint32_t full_bar(uint32_t bars, int j, int s) {
 __device__ __forceinline__ uint32_t q_empty_bar(uint32_t bars, int W, int j) {
   return bars + 8u * static_cast<uint32_t>(2 * W * kStages + j);
 }
+// Append: consumer j has taken the latest raw K and V rows of its query slot.
+__device__ __forceinline__ uint32_t r_empty_bar(uint32_t bars, int W, int j) {
+  return bars + 8u * static_cast<uint32_t>(2 * W * kStages + W + j);
+}
 
 // ---------------------------------------------------------------- producer warp
 
@@ -207,6 +217,7 @@ __device__ __forceinline__ void cursor_next(Cursor& u, const DecodeArgs& a) {
 // "q empty" barrier). A consumer whose range is empty gets one descriptor with
 // n = 0 and the last bit. The block ids of the next chunk are loaded when the
 // current one is issued, so their latency overlaps the wait for a free stage.
+template <bool APPEND>
 __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, uint32_t qslots, uint32_t first,
                               uint32_t lut, uint32_t klut) {
   // Everything that may read what the previous kernel wrote comes after
@@ -309,7 +320,7 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
   }
 
   // the next chunk to issue (planned one chunk ahead, block ids in flight)
-  int n_n = 0, n_seg = 0, n_len = 0, n_b = 0, n_h = 0, n_t = 0;
+  int n_n = 0, n_seg = 0, n_len = 0, n_b = 0, n_h = 0, n_t = 0, n_raw = -1;
   int n_blk[kChunk];
 #pragma unroll
   for (int i = 0; i < kChunk; ++i) n_blk[i] = -1;
@@ -322,6 +333,9 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
     n_h = pc.h;
     n_t = pc.t;
     n_len = pc.len;
+    // append: the raw length of a sequence whose last tile this chunk holds
+    // (a clamped length has no newest token to store)
+    if constexpr (APPEND) n_raw = pc.t + n == pc.nt ? ld_dep_s32(a.seq_lens + pc.b) : -1;
     n_seg = (pc.b * a.n_kv + pc.h) * a.num_parts + (a.part_tiles > 0 ? pc.t / a.part_tiles : 0);
     const int* row = a.block_table + static_cast<long long>(pc.b) * a.bt_stride;
 #pragma unroll
@@ -338,8 +352,10 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
   // stage_at without its division: stages [0, nb_front) lie before the LUT
   const uint32_t nb_front = klut && lut > first ? (lut - first) / a.stage_bytes : (klut ? 0u : 0xFFFFFFFFu);
   const uint32_t back = lut + klut;
-  const uint32_t qslot = qslots + static_cast<uint32_t>(mine ? jc : 0) * a.qbuf_bytes;
+  const uint32_t qslot = qslots + static_cast<uint32_t>(mine ? jc : 0) * a.qslot_bytes;
   const uint32_t qbar = q_empty_bar(bars, W, mine ? jc : 0);
+  const uint32_t rbar = r_empty_bar(bars, W, mine ? jc : 0);
+  int rn = 0, rdone = 0;                    // raw-row copies issued / known consumed
   uint32_t eparity = (1u << kStages) - 1;   // empty-barrier parity to wait for, per stage
   uint32_t used = 0, fpar = 0;              // stages ever filled; parity of their next fill
   int ps = 0, prev_seg = -1;
@@ -352,9 +368,24 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
     // chunk are only read on the next pass, after other lanes' work
     for (int pass = 0; pass < TQ_PRODUCER_PASSES && !done; ++pass) {
       const bool newq = n_n > 0 && n_seg != prev_seg;
+      // append: the newest position's tile is in this chunk (its block id in
+      // range) and the length was not cut: the raw K and V rows go into the
+      // query slot after the query rows (their own "taken" barrier)
+      bool app = false;
+      if constexpr (APPEND) {
+        const int app_i = n_len - 1 - n_t * kTileTokens >= 0 ? (n_len - 1 - n_t * kTileTokens) >> 4 : kChunk;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i)
+          if (i == app_i) app = i < n_n && n_blk[i] >= 0 && n_blk[i] < a.num_blocks;
+        app = app && n_raw > 0 && n_raw == n_len;
+      }
       if (newq && qdone < qn) {   // the slot still holds rows the consumer has not taken
         if (!mbar_test(qbar, (qn - 1) & 1)) break;
         qdone = qn;
+      }
+      if (APPEND && app && rdone < rn) {    // the same for the raw rows
+        if (!mbar_test(rbar, (rn - 1) & 1)) break;
+        rdone = rn;
       }
       const uint32_t fb = full_bar(bars, jc, ps);
       if (!mbar_test(fb + 8, (eparity >> ps) & 1u)) break;
@@ -370,10 +401,11 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
           bytes += a.tile_bytes;
         }
       if (newq) bytes += a.qbuf_bytes;
+      if (APPEND && app) bytes += 2 * kRawRowBytes;
       sts128(sa + a.desc_off, make_uint4(static_cast<uint32_t>(n_seg), static_cast<uint32_t>(n_t << 4),
                                          static_cast<uint32_t>(n_len),
                                          static_cast<uint32_t>(n_n) | (okm << 4) | (last ? 256u : 0u) |
-                                             (newq ? 512u : 0u)));
+                                             (newq ? 512u : 0u) | (APPEND && app ? kAppendBit : 0u)));
       // No proxy fence: the consumer's reads of the stage are ordered before
       // these copies by its arrive on the empty barrier (release) and the
       // test above (acquire); the descriptor goes generic store -> generic load
@@ -387,12 +419,19 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
                                    static_cast<uint32_t>(a.tile_bytes);
           bulk_g2s(sa + i * a.tile_bytes, src, a.tile_bytes, fb, policy);
         }
+      if (APPEND && app) {
+        const long long row = (static_cast<long long>(n_b) * a.n_kv + n_h) * kRawRowBytes;
+        const uint32_t dst = qslot + static_cast<uint32_t>(a.qbuf_bytes);
+        bulk_g2s_plain(dst, static_cast<const uint8_t*>(a.new_k) + row, kRawRowBytes, fb);
+        bulk_g2s_plain(dst + kRawRowBytes, static_cast<const uint8_t*>(a.new_v) + row, kRawRowBytes, fb);
+      }
       if (newq) {
         const uint8_t* src = static_cast<const uint8_t*>(a.q) +
                              (static_cast<long long>(n_b) * a.n_q + n_h * a.group) * (kD * 2);
         bulk_g2s_plain(qslot, src, a.qbuf_bytes, fb);
         ++qn;
       }
+      if (APPEND && app) ++rn;
       if (n_n > 0) prev_seg = n_seg;
       used |= 1u << ps;
       fpar ^= 1u << ps;
@@ -419,6 +458,54 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
       if ((used >> s) & 1u) mbar_wait(full_bar(bars, jc, s), ((fpar >> s) & 1u) ^ 1u);
 }
 
+// ---------------------------------------------------------------- append
+
+// The newest token of the stage's segment (position len - 1, in tile i of the
+// stage, row r): the warp quantises its raw key and value rows (in the query
+// slot at `raw`; the key in the first half, the value in the second) with the
+// store's arithmetic, writes
+// the bytes into the cache tile in global memory and patches the same row of
+// the stage's copy, which the bulk copy brought with the row's old bytes. The
+// patch goes through the generic proxy; the fence orders it before the
+// stage's next bulk fill (async proxy) once the consumer releases the stage.
+template <int KMODE, int VBITS, typename TQ>
+__device__ __forceinline__ void append_newest(const DecodeArgs& a, uint32_t sa, uint4 desc, int lane, uint32_t raw,
+                                           uint32_t codebook) {
+  const int len = static_cast<int>(desc.z), tok0 = static_cast<int>(desc.y);
+  const int p = len - 1;
+  const int i = (p - tok0) >> 4, r = p & (kTileTokens - 1);
+  const int bh = static_cast<int>(desc.x) / a.num_parts;
+  const int b = bh / a.n_kv, h = bh - b * a.n_kv;
+  // the producer found this block id in range; its load overlaps the quantisation
+  const long long blk = ld_dep_s32(a.block_table + static_cast<long long>(b) * a.bt_stride + (p >> a.log2_bs));
+  const int l = lane & 15;
+  const TileGeom g = {a.k_off, a.k_row, a.v_off, a.v_row, a.knorm_off, a.vscale_off, a.vzero_off};
+  uint8_t* gtile = a.wcache + (blk * a.n_kv + h) * a.tiles_per_block * static_cast<long long>(a.tile_bytes) +
+                   static_cast<long long>((p >> 4) & (a.tiles_per_block - 1)) * a.tile_bytes;
+  uint8_t* stile = static_cast<uint8_t*>(__cvta_shared_to_generic(sa + static_cast<uint32_t>(i * a.tile_bytes)));
+  const float* mid = static_cast<const float*>(__cvta_shared_to_generic(codebook));
+  const float* cent = mid + 16;
+  // the first half quantises the key, the second the value, at the same time
+  const bool kh = lane < 16;
+  const unsigned hm = kh ? 0x0000ffffu : 0xffff0000u;
+  const uint32_t row = raw + (kh ? 0u : kRawRowBytes) + 16u * static_cast<uint32_t>(l);
+  PairBytes o;
+  float x[8];
+  u2_to_f4<TQ>(lds64(row), x);
+  u2_to_f4<TQ>(lds64(row + 8), x + 4);
+  if (kh) {
+    quantize_key<KMODE>(x, l, mid, cent, o, hm);
+    write_key<KMODE>(gtile, r, g, l, o);
+    write_key<KMODE>(stile, r, g, l, o);
+  } else {
+    quantize_value<VBITS>(x, o, hm);
+    write_value<VBITS>(gtile, r, g, l, o);
+    write_value<VBITS>(stile, r, g, l, o);
+  }
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  __syncwarp();
+}
+
 // ---------------------------------------------------------------- consumer warps
 
 // Consumer warp j: takes its ring stages in order and runs the attention math
@@ -428,7 +515,7 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
 //     2 (c & 1), 2 (c & 1) + 1 and one exchange gives both the full score.
 //   G > 4: column k is head k; the lo parts run in a second mma into the same
 //     accumulators.
-template <int KMODE, int GBIG, int VBITS, typename TQ>
+template <int KMODE, int GBIG, int VBITS, typename TQ, bool APPEND>
 __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, uint32_t qslots, uint32_t first,
                               uint32_t lut,
                               uint32_t klut) {
@@ -807,13 +894,21 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
       const int seg = static_cast<int>(desc.x);
       if (seg != c_seg) {
         if (c_seg >= 0) finalize(c_seg);
-        begin_segment(qslots + static_cast<uint32_t>(j) * a.qbuf_bytes);
+        begin_segment(qslots + static_cast<uint32_t>(j) * a.qslot_bytes);
         __syncwarp();   // every lane has read the query slot: the producer may refill it
         if (lane == 0) mbar_arrive(q_empty_bar(bars, W, j));
         c_seg = seg;
       }
       const int tok0 = static_cast<int>(desc.y), len = static_cast<int>(desc.z);
       if (okm != (1u << n) - 1 && lane == 0) flag(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
+      if constexpr (APPEND) {
+        if (desc.w & kAppendBit) {
+          const uint32_t slot = qslots + static_cast<uint32_t>(j) * a.qslot_bytes;
+          append_newest<KMODE, VBITS, TQ>(a, sa, desc, lane, slot + static_cast<uint32_t>(a.qbuf_bytes),
+                                          bars + kCodebookOff);
+          if (lane == 0) mbar_arrive(r_empty_bar(bars, W, j));   // append_newest ends with __syncwarp
+        }
+      }
       int nv[kChunk];
 #pragma unroll
       for (int i = 0; i < kChunk; ++i)
@@ -845,7 +940,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
 
 // Warps 0 .. kProducers - 1 are producers; the rest are the W consumers. One
 // CTA per SM.
-template <int KMODE, int GBIG, int VBITS, typename TQ>
+template <int KMODE, int GBIG, int VBITS, typename TQ, bool APPEND>
 __global__ void __launch_bounds__((kMaxConsumers + kProducers) * 32, 1)
 split_kernel(const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t s_dyn[];
@@ -854,7 +949,7 @@ split_kernel(const DecodeArgs a) {
   const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(s_dyn));
   const uint32_t end = base + static_cast<uint32_t>(a.dyn_bytes);
   constexpr uint32_t kLut = lut_bytes<KMODE>();
-  const uint32_t head = kBarHead + static_cast<uint32_t>(W) * a.qbuf_bytes;
+  const uint32_t head = kBarHead + static_cast<uint32_t>(W) * a.qslot_bytes;
   const uint32_t lut = kLut ? lut_at(base, kLut, head) : end;
   const uint32_t bars = base;
   const uint32_t qslots = base + kBarHead;
@@ -874,19 +969,24 @@ split_kernel(const DecodeArgs a) {
   if (warp < kProducers) {
     if (warp == 0) {
       const int lane = threadIdx.x & 31;
-      for (int i = lane; i < 2 * W * kStages + W; i += 32) mbar_init(bars + 8 * i, 1);
+      for (int i = lane; i < 2 * W * kStages + (APPEND ? 2 : 1) * W; i += 32) mbar_init(bars + 8 * i, 1);
       asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (kProducers > 1) asm volatile("bar.sync 2, %0;\n" ::"r"(kProducers * 32) : "memory");   // barriers exist
     else __syncwarp();
-    producer_warp(a, W, warp, bars, qslots, first, lut, kLut);   // waits for the previous kernel itself
+    producer_warp<APPEND>(a, W, warp, bars, qslots, first, lut, kLut);   // waits for the previous kernel itself
   } else {
     constexpr int kP = kProducers * 32;
     if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent, threadIdx.x - kP, blockDim.x - kP);
+    if (APPEND && threadIdx.x - kP < 32) {   // the key codebook of the append path
+      const int i = threadIdx.x - kP;
+      const float v = i < 16 ? (i < 15 ? a.mid[i] : 0.f) : a.scent[i - 16];
+      asm volatile("st.shared.f32 [%0], %1;\n" ::"r"(bars + kCodebookOff + 4u * i), "f"(v) : "memory");
+    }
     asm volatile("bar.sync 1, %0;\n" ::"r"(blockDim.x) : "memory");
     grid_dep_wait();   // already resolved: the producers passed it before arriving
     grid_dep_launch();
-    consumer_warp<KMODE, GBIG, VBITS, TQ>(a, W, warp - kProducers, bars, qslots, first, lut, kLut);
+    consumer_warp<KMODE, GBIG, VBITS, TQ, APPEND>(a, W, warp - kProducers, bars, qslots, first, lut, kLut);
   }
 }
 
@@ -1248,6 +1348,7 @@ struct LaunchShape {
   int consumers;    // consumer warps per CTA (one producer warp besides)
   int stage_bytes;
   int desc_off;
+  int qslot_bytes;
   int dyn_bytes;
 };
 
@@ -1266,7 +1367,7 @@ int consumers_that_fit(uint32_t start, uint32_t dyn, uint32_t klut, uint32_t sb,
 }
 
 template <int KMODE>
-bool launch_shape(int tile_bytes, int group, LaunchShape* s) {
+bool launch_shape(int tile_bytes, int group, bool append, LaunchShape* s) {
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return false;
@@ -1274,7 +1375,8 @@ bool launch_shape(int tile_bytes, int group, LaunchShape* s) {
   s->stage_bytes = (s->desc_off + 16 + 127) & ~127;
   const uint32_t klut = lut_bytes<KMODE>();
   // the window may start at 0 or after a small reserved area; take the worse
-  const uint32_t qbytes = static_cast<uint32_t>(group) * kD * 2;
+  const uint32_t qbytes = static_cast<uint32_t>(group) * kD * 2 + (append ? 2 * kRawRowBytes : 0u);
+  s->qslot_bytes = static_cast<int>(qbytes);
   int w = consumers_that_fit(0, optin, klut, s->stage_bytes, qbytes);
   const int w2 = consumers_that_fit(1024, optin, klut, s->stage_bytes, qbytes);
   if (w2 < w) w = w2;
@@ -1284,44 +1386,54 @@ bool launch_shape(int tile_bytes, int group, LaunchShape* s) {
   return true;
 }
 
-template <int KMODE, int GBIG, int VBITS, typename TQ>
+template <int KMODE, int GBIG, int VBITS, typename TQ, bool APPEND>
 cudaError_t launch_split_typed(DecodeArgs a, cudaStream_t s, int sms) {
   LaunchShape sh;
-  if (!launch_shape<KMODE>(a.tile_bytes, a.group, &sh)) return cudaErrorInvalidConfiguration;
+  if (!launch_shape<KMODE>(a.tile_bytes, a.group, a.new_k != nullptr, &sh)) return cudaErrorInvalidConfiguration;
   a.stage_bytes = sh.stage_bytes;
   a.desc_off = sh.desc_off;
+  a.qslot_bytes = sh.qslot_bytes;
   a.dyn_bytes = sh.dyn_bytes;
   a.qbuf_bytes = a.group * kD * 2;
-  auto k = split_kernel<KMODE, GBIG, VBITS, TQ>;
+  auto k = split_kernel<KMODE, GBIG, VBITS, TQ, APPEND>;
   cudaError_t err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, a.dyn_bytes);
   if (err != cudaSuccess) return err;
   return launch_pdl(k, dim3(static_cast<unsigned>(sms)), dim3((sh.consumers + kProducers) * 32),
                     static_cast<size_t>(a.dyn_bytes), s, a);
 }
 
+// The append variant is a separate instance, so the plain decode's kernel is
+// compiled without any of its code.
+template <int KMODE, int GBIG, int VBITS, typename TQ>
+cudaError_t launch_split_append(const DecodeArgs& a, cudaStream_t s, int sms) {
+  return a.new_k ? launch_split_typed<KMODE, GBIG, VBITS, TQ, true>(a, s, sms)
+                 : launch_split_typed<KMODE, GBIG, VBITS, TQ, false>(a, s, sms);
+}
+
 template <int KMODE, int VBITS>
 cudaError_t launch_split(const DecodeArgs& a, int q_dtype, cudaStream_t s, int sms) {
   if (q_dtype == TQ_DTYPE_BF16)
-    return a.group > 4 ? launch_split_typed<KMODE, 1, VBITS, __nv_bfloat16>(a, s, sms)
-                       : launch_split_typed<KMODE, 0, VBITS, __nv_bfloat16>(a, s, sms);
-  return a.group > 4 ? launch_split_typed<KMODE, 1, VBITS, __half>(a, s, sms)
-                     : launch_split_typed<KMODE, 0, VBITS, __half>(a, s, sms);
+    return a.group > 4 ? launch_split_append<KMODE, 1, VBITS, __nv_bfloat16>(a, s, sms)
+                       : launch_split_append<KMODE, 0, VBITS, __nv_bfloat16>(a, s, sms);
+  return a.group > 4 ? launch_split_append<KMODE, 1, VBITS, __half>(a, s, sms)
+                     : launch_split_append<KMODE, 0, VBITS, __half>(a, s, sms);
 }
 
 // Consumer warps per CTA of the split launch (the reduce needs the count).
-int split_warps_per_cta(const tq_layout& L, int group) {
+int split_warps_per_cta(const tq_layout& L, int group, bool append) {
   LaunchShape sh;
   bool ok;
-  if (L.key_fp8) ok = launch_shape<kFp8>(L.tile_bytes, group, &sh);
-  else if (L.key_bits == 4) ok = launch_shape<kMse4>(L.tile_bytes, group, &sh);
-  else ok = launch_shape<kMse3>(L.tile_bytes, group, &sh);
+  if (L.key_fp8) ok = launch_shape<kFp8>(L.tile_bytes, group, append, &sh);
+  else if (L.key_bits == 4) ok = launch_shape<kMse4>(L.tile_bytes, group, append, &sh);
+  else ok = launch_shape<kMse3>(L.tile_bytes, group, append, &sh);
   return ok ? sh.consumers : 0;
 }
 
 tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* q, int q_dtype,
                        const void* cache, long long num_blocks, const int* block_table, int bt_stride,
                        const int* seq_lens, int batch, int max_seq_len, float scale, void* workspace,
-                       size_t ws_bytes, unsigned int* dev_status, cudaStream_t stream) {
+                       size_t ws_bytes, unsigned int* dev_status, cudaStream_t stream,
+                       const void* new_k = nullptr, const void* new_v = nullptr) {
   if (bt_stride < 1) return TQ_ERR_INVALID_ARG;
   Plan P;
   tq_status st = make_plan(cfg, batch, max_seq_len, bt_stride, false, &P);
@@ -1338,6 +1450,8 @@ tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* 
     return TQ_ERR_MISALIGNED;
   if (dev_status && (reinterpret_cast<unsigned long long>(dev_status) & 3ull)) return TQ_ERR_MISALIGNED;
   if (num_blocks < 0) return TQ_ERR_INVALID_ARG;
+  if ((new_k == nullptr) != (new_v == nullptr)) return TQ_ERR_INVALID_ARG;
+  if (new_k && (!aligned16(new_k) || !aligned16(new_v))) return TQ_ERR_MISALIGNED;
   make_plan(cfg, batch, max_seq_len, bt_stride, true, &P);
   if (P.sms <= 0) return TQ_ERR_CUDA;
 
@@ -1380,6 +1494,14 @@ tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* 
   a.qscale /= gamma;
   for (int i = 0; i < 16; ++i)
     a.cent[i] = (!P.L.key_fp8 && i < cb->num_levels) ? static_cast<float>(static_cast<double>(gamma) * cb->centroids[i]) : 0.f;
+  a.new_k = new_k;
+  a.new_v = new_v;
+  a.wcache = new_k ? static_cast<uint8_t*>(const_cast<void*>(cache)) : nullptr;
+  a.qslot_bytes = 0;
+  a.k_row = P.L.k_row_bytes;
+  a.v_row = P.L.v_row_bytes;
+  for (int i = 0; i < 15; ++i) a.mid[i] = (!P.L.key_fp8 && i < cb->num_levels - 1) ? cb->midpoints[i] : 0.f;
+  for (int i = 0; i < 16; ++i) a.scent[i] = (!P.L.key_fp8 && i < cb->num_levels) ? cb->centroids[i] : 0.f;
 
   cudaError_t err;
   if (P.L.key_fp8) err = launch_split<kFp8, 4>(a, q_dtype, stream, P.sms);
@@ -1391,7 +1513,7 @@ tq_status run_partials(const tq_config* cfg, const tq_codebook* cb, const void* 
 
 tq_status run_reduce(const tq_config* cfg, const int* seq_lens, int batch, int max_seq_len, int bt_stride,
                      void* out, int out_dtype, const void* workspace, size_t ws_bytes, cudaStream_t stream,
-                     bool after_split) {
+                     bool after_split, bool append = false) {
   if (bt_stride < 1) return TQ_ERR_INVALID_ARG;
   Plan P;
   tq_status st = make_plan(cfg, batch, max_seq_len, bt_stride, false, &P);
@@ -1405,7 +1527,7 @@ tq_status run_reduce(const tq_config* cfg, const int* seq_lens, int batch, int m
   make_plan(cfg, batch, max_seq_len, bt_stride, true, &P);
   if (P.sms <= 0) return TQ_ERR_CUDA;
   const int G = cfg->num_q_heads / cfg->num_kv_heads;
-  const int warps = split_warps_per_cta(P.L, G);
+  const int warps = split_warps_per_cta(P.L, G, append);
   if (warps <= 0) return TQ_ERR_CUDA;
   ReduceArgs r;
   r.seq_lens = seq_lens;
@@ -1481,6 +1603,24 @@ tq_status tq_decode(const tq_config* cfg, const tq_codebook* cb, const void* q, 
   if (st != TQ_OK) return st;
   return tq::run_reduce(cfg, seq_lens, batch, max_seq_len, bt_stride, out, out_dtype, workspace,
                         workspace_bytes, s, true);
+}
+
+tq_status tq_decode_append(const tq_config* cfg, const tq_codebook* cb, const void* q, int q_dtype,
+                           const void* new_k, const void* new_v, void* cache, long long num_blocks,
+                           const int* block_table, int bt_stride, const int* seq_lens, int batch, int max_seq_len,
+                           float scale, void* out, int out_dtype, void* workspace, size_t workspace_bytes,
+                           unsigned int* dev_status, tq_stream_t stream) {
+  if (out_dtype != TQ_DTYPE_F16 && out_dtype != TQ_DTYPE_BF16 && out_dtype != TQ_DTYPE_F32)
+    return TQ_ERR_INVALID_ARG;
+  if (batch > 0 && (!out || !new_k || !new_v)) return TQ_ERR_INVALID_ARG;
+  if (batch > 0 && !tq::aligned16(out)) return TQ_ERR_MISALIGNED;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  tq_status st = tq::run_partials(cfg, cb, q, q_dtype, cache, num_blocks, block_table, bt_stride, seq_lens,
+                                  batch, max_seq_len, scale, workspace, workspace_bytes, dev_status, s,
+                                  new_k, new_v);
+  if (st != TQ_OK) return st;
+  return tq::run_reduce(cfg, seq_lens, batch, max_seq_len, bt_stride, out, out_dtype, workspace,
+                        workspace_bytes, s, true, true);
 }
 
 }  // extern "C"

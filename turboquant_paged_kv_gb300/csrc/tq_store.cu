@@ -33,6 +33,7 @@
 
 #include "tq_internal.h"
 #include "tq_launch.cuh"
+#include "tq_store.cuh"
 #include "tq_vec.cuh"
 
 namespace tq {
@@ -64,38 +65,10 @@ struct StoreArgs {
 };
 
 
-enum KeyMode { kMse4 = 4, kMse3 = 3, kFp8 = 8 };
+enum KeyMode { kMse4 = 4, kMse3 = 3, kFp8 = 8 };   // the key codes' bits (8: e4m3)
 
 __device__ __forceinline__ void flag(unsigned int* status, unsigned int bit) {
   if (status) atomicOr(status, bit);
-}
-
-// Codes of 8 values of one vector: trunc(fp32((v - min) / s) + 1/2), clamped
-// to [0, kLevels], with IEEE division as specified. The product with an
-// approximate reciprocal is within 4e-6 of the quotient (t <= 15), so
-// away from a rounding boundary it gives the same code; a value within 1e-5
-// of one takes the exact quotient, on a branch that is rarely taken (the
-// division is a long instruction sequence, so it must not run for every
-// coordinate).
-template <int kLevels>
-__device__ __forceinline__ void value_codes(const float v[8], float mn, float s, int q[8]) {
-  const float rs = __fdividef(1.f, s);   // approximate: within a few ulp, far inside the band
-  float dv[8];
-  uint32_t near = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    dv[j] = __fsub_rn(v[j], mn);
-    const float u = fmaf(dv[j], rs, 0.5f);
-    near |= fabsf(u - rintf(u)) < 1e-5f ? (1u << j) : 0u;
-    q[j] = __float2int_rz(u);
-  }
-  if (near) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if ((near >> j) & 1u) q[j] = __float2int_rz(__fadd_rn(__fdiv_rn(dv[j], s), 0.5f));
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) q[j] = min(q[j], kLevels);   // v >= min, so no code is negative
 }
 
 // Warp w of the CTA handles vectors 2 w and 2 w + 1 of the CTA's 16, one per
@@ -154,107 +127,12 @@ store_kernel(const StoreArgs a) {
     }
   }
 
-  // ---------------- keys ----------------
-  if constexpr (KMODE == kFp8) {
-    uint32_t w[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(k[4 * i], k[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
-      const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(k[4 * i + 2], k[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
-      w[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-    }
-    if (live) *reinterpret_cast<uint2*>(tile + a.k_off + r * a.k_row + 8 * l) = make_uint2(w[0], w[1]);
-  } else {
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) ss = fmaf(k[j], k[j], ss);
-    // The key's scalars use the hardware approximations (a few ulp): the
-    // pages' own pipeline forms y in fp32 through a matrix product, so y is
-    // only defined to fp32 rounding, and the index decisions are checked
-    // against the exact value with a 1e-5 band; the stored norm is an fp16.
-    const float ss16 = half_sum(ss);
-    const float n = ss16 > 0.f ? ss16 * rsqrtf(ss16) : 0.f;
-    fwht128_half(k, l);
-    const float sc = __fdividef(0.088388347648318440f, n + 1e-8f);   // 1/sqrt(128) / (n + 1e-8)
-    int idx[8];
-    float cs = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float y = k[j] * sc;
-      // #{m : y >= mid_m} over the ascending midpoints, by binary search
-      int c = 0;
-#pragma unroll
-      for (int step = 1 << (KMODE - 1); step >= 1; step >>= 1) c += (y >= s_mid[c + step - 1]) ? step : 0;
-      idx[j] = c;
-      const float cv = s_cent[c];
-      cs = fmaf(cv, cv, cs);
-    }
-    cs = half_sum(cs);
-    const float stored = n * rsqrtf(cs + 1e-16f);
-    uint32_t w = 0;   // LSB-first: coordinate 8 l + j at bit KMODE * j of the lane's run
-#pragma unroll
-    for (int j = 0; j < 8; ++j) w |= static_cast<uint32_t>(idx[j]) << (KMODE * j);
-    if (live) {
-      uint8_t* row = tile + a.k_off + r * a.k_row;
-      if constexpr (KMODE == kMse4) {
-        *reinterpret_cast<uint32_t*>(row + 4 * l) = w;
-      } else {   // 3 bytes at 3 l
-        row[3 * l] = static_cast<uint8_t>(w);
-        row[3 * l + 1] = static_cast<uint8_t>(w >> 8);
-        row[3 * l + 2] = static_cast<uint8_t>(w >> 16);
-      }
-      if (l == 0)
-        *reinterpret_cast<uint16_t*>(tile + a.knorm_off + 2 * r) = __half_as_ushort(__float2half_rn(stored));
-    }
-  }
-
-  // ---------------- values ----------------
-  constexpr int kLevels = (1 << VBITS) - 1;
-  float mn = v[0], mx = v[0];
-#pragma unroll
-  for (int j = 1; j < 8; ++j) {
-    mn = fminf(mn, v[j]);
-    mx = fmaxf(mx, v[j]);
-  }
-  mn = half_min(mn);
-  mx = half_max(mx);
-  float s = __fdiv_rn(__fsub_rn(mx, mn), static_cast<float>(kLevels));
-  s = (s > 1e-8f) ? s : 1e-8f;
-  int q[8];
-  value_codes<kLevels>(v, mn, s, q);
-  uint32_t w = 0;   // this lane's LSB-first run: coordinate 8 l + j at bit VBITS * j
-#pragma unroll
-  for (int j = 0; j < 8; ++j) w |= static_cast<uint32_t>(q[j]) << (VBITS * j);
-  // Pair-interleaved 16-bit words: word i of token r = 2 p + t sits at
-  // v_off + 2 p v_row + 16 ((i >> 2) ^ x) + 4 (i & 3) + 2 t, x = 2 (p & 3) when
-  // v_row is a multiple of 64, else 0.
-  const int pair = r >> 1;
-  const int swz = (a.v_row % 64 == 0) ? 2 * (pair & 3) : 0;
-  uint8_t* vbase = live ? tile + a.v_off + pair * 2 * a.v_row + 2 * (r & 1) : nullptr;
-  auto put_word = [&](int i, uint32_t bits16) {
-    *reinterpret_cast<uint16_t*>(vbase + 16 * ((i >> 2) ^ swz) + 4 * (i & 3)) = static_cast<uint16_t>(bits16);
-  };
-  if constexpr (VBITS == 4) {   // lane l holds words 2 l and 2 l + 1
-    if (live) {
-      put_word(2 * l, w);
-      put_word(2 * l + 1, w >> 16);
-    }
-  } else {   // 3-bit: lanes 2 m, 2 m + 1 hold the 48 bits of words 3 m .. 3 m + 2
-    const uint32_t other = __shfl_xor_sync(0xffffffffu, w, 1);
-    if (live) {
-      const int m = l >> 1;
-      if ((l & 1) == 0) {
-        put_word(3 * m, w);                                      // bits 0-15
-        put_word(3 * m + 1, (w >> 16) | ((other & 0xFFu) << 8));  // bits 16-23 | partner's 0-7
-      } else {
-        put_word(3 * m + 2, w >> 8);                             // bits 8-23
-      }
-    }
-  }
-  if (live && l == 0) {
-    *reinterpret_cast<uint16_t*>(tile + a.vscale_off + 2 * r) = __half_as_ushort(__float2half_rn(s));
-    *reinterpret_cast<uint16_t*>(tile + a.vzero_off + 2 * r) = __half_as_ushort(__float2half_rn(mn));
-  }
+  const TileGeom geom = {a.k_off, a.k_row, a.v_off, a.v_row, a.knorm_off, a.vscale_off, a.vzero_off};
+  PairBytes o;
+  quantize_key<KMODE>(k, l, s_mid, s_cent, o);
+  if (live) write_key<KMODE>(tile, r, geom, l, o);
+  quantize_value<VBITS>(v, o);
+  if (live) write_value<VBITS>(tile, r, geom, l, o);
 }
 
 template <int KMODE, int VBITS>

@@ -30,20 +30,22 @@ __device__ __forceinline__ void load8(const void* base, long long elem, float ou
   }
 }
 
-// Sum, min and max over the 16 lanes of a half-warp (xor 1 .. 8 stay inside it).
-__device__ __forceinline__ float half_sum(float x) {
+// Sum, min and max over the 16 lanes of a half-warp (xor 1 .. 8 stay inside
+// it). `mask` names the lanes that take part: the whole warp, or one half when
+// the two halves run different code.
+__device__ __forceinline__ float half_sum(float x, unsigned mask = 0xffffffffu) {
 #pragma unroll
-  for (int m = 1; m <= 8; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+  for (int m = 1; m <= 8; m <<= 1) x += __shfl_xor_sync(mask, x, m);
   return x;
 }
-__device__ __forceinline__ float half_min(float x) {
+__device__ __forceinline__ float half_min(float x, unsigned mask = 0xffffffffu) {
 #pragma unroll
-  for (int m = 1; m <= 8; m <<= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, m));
+  for (int m = 1; m <= 8; m <<= 1) x = fminf(x, __shfl_xor_sync(mask, x, m));
   return x;
 }
-__device__ __forceinline__ float half_max(float x) {
+__device__ __forceinline__ float half_max(float x, unsigned mask = 0xffffffffu) {
 #pragma unroll
-  for (int m = 1; m <= 8; m <<= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, m));
+  for (int m = 1; m <= 8; m <<= 1) x = fmaxf(x, __shfl_xor_sync(mask, x, m));
   return x;
 }
 
@@ -51,7 +53,7 @@ __device__ __forceinline__ float half_max(float x) {
 // coordinates of a half-warp, coordinate 8 l + j in lane l: index bits 0-2 in
 // the lane, bits 3-6 across lanes l ^ 1 .. l ^ 8. The lane whose stride bit is
 // set keeps (partner - own), the other (own + partner).
-__device__ __forceinline__ void fwht128_half(float v[8], int l) {
+__device__ __forceinline__ void fwht128_half(float v[8], int l, unsigned mask = 0xffffffffu) {
 #pragma unroll
   for (int h = 1; h < 8; h <<= 1) {
 #pragma unroll
@@ -66,7 +68,7 @@ __device__ __forceinline__ void fwht128_half(float v[8], int l) {
   for (int m = 1; m <= 8; m <<= 1) {
     const float sgn = (l & m) ? -1.f : 1.f;   // one exact fma with +-1 per step
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = fmaf(sgn, v[j], __shfl_xor_sync(0xffffffffu, v[j], m));
+    for (int j = 0; j < 8; ++j) v[j] = fmaf(sgn, v[j], __shfl_xor_sync(mask, v[j], m));
   }
 }
 

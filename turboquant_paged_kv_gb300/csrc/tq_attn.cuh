@@ -42,7 +42,7 @@ struct DecodeArgs {
   int stage_bytes;     // ring stage: kChunk tiles, then the descriptor
   int desc_off;        // offset of the descriptor in a stage
   int qbuf_bytes;      // G * d * 2: the query rows of a segment
-  int qslot_bytes;     // a consumer's query slot: the query rows, then (append) the raw K and V rows
+  int qslot_bytes;     // a consumer's query slot: the query rows, then (append) two halves of raw K and V rows
   int dyn_bytes;
   float qscale;        // softmax scale * log2(e)
   int early_indices;   // TQ_FLAG_INDICES_READY: lengths and block ids read before the dependency wait

@@ -133,9 +133,8 @@ static_assert(kMaxConsumers + kProducers <= 12, "12 warps keep 168 registers per
 // G * d * 2 bytes per consumer.
 constexpr uint32_t kBarHead = 1024;
 constexpr uint32_t kCodebookOff = kBarHead - 128;
-static_assert((2 * kMaxConsumers * kStages + 2 * kMaxConsumers) * 8 <= static_cast<int>(kCodebookOff), "barrier area");
-constexpr uint32_t kAppendBit = 1024;   // descriptor: the stage carries the newest token's raw K and V rows
-constexpr uint32_t kRawRowBytes = kD * 2;
+static_assert((2 * kMaxConsumers * kStages + kMaxConsumers) * 8 <= static_cast<int>(kCodebookOff), "barrier area");
+constexpr uint32_t kRawRowBytes = kD * 2;   // append: one raw key or value row (f16 / bf16)
 static_assert(kStages >= 2 && kChunk >= 1 && kChunk <= 4, "ring shape");
 
 // ---------------------------------------------------------------- ring plan
@@ -182,10 +181,6 @@ __device__ __forceinline__ uint32_t full_bar(uint32_t bars, int j, int s) {
 __device__ __forceinline__ uint32_t q_empty_bar(uint32_t bars, int W, int j) {
   return bars + 8u * static_cast<uint32_t>(2 * W * kStages + j);
 }
-// Append: consumer j has taken the latest raw K and V rows of its query slot.
-__device__ __forceinline__ uint32_t r_empty_bar(uint32_t bars, int W, int j) {
-  return bars + 8u * static_cast<uint32_t>(2 * W * kStages + W + j);
-}
 
 // ---------------------------------------------------------------- producer warp
 
@@ -217,7 +212,6 @@ __device__ __forceinline__ void cursor_next(Cursor& u, const DecodeArgs& a) {
 // "q empty" barrier). A consumer whose range is empty gets one descriptor with
 // n = 0 and the last bit. The block ids of the next chunk are loaded when the
 // current one is issued, so their latency overlaps the wait for a free stage.
-template <bool APPEND>
 __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, uint32_t qslots, uint32_t first,
                               uint32_t lut, uint32_t klut) {
   // Everything that may read what the previous kernel wrote comes after
@@ -320,7 +314,7 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
   }
 
   // the next chunk to issue (planned one chunk ahead, block ids in flight)
-  int n_n = 0, n_seg = 0, n_len = 0, n_b = 0, n_h = 0, n_t = 0, n_raw = -1;
+  int n_n = 0, n_seg = 0, n_len = 0, n_b = 0, n_h = 0, n_t = 0;
   int n_blk[kChunk];
 #pragma unroll
   for (int i = 0; i < kChunk; ++i) n_blk[i] = -1;
@@ -333,9 +327,6 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
     n_h = pc.h;
     n_t = pc.t;
     n_len = pc.len;
-    // append: the raw length of a sequence whose last tile this chunk holds
-    // (a clamped length has no newest token to store)
-    if constexpr (APPEND) n_raw = pc.t + n == pc.nt ? ld_dep_s32(a.seq_lens + pc.b) : -1;
     n_seg = (pc.b * a.n_kv + pc.h) * a.num_parts + (a.part_tiles > 0 ? pc.t / a.part_tiles : 0);
     const int* row = a.block_table + static_cast<long long>(pc.b) * a.bt_stride;
 #pragma unroll
@@ -354,8 +345,6 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
   const uint32_t back = lut + klut;
   const uint32_t qslot = qslots + static_cast<uint32_t>(mine ? jc : 0) * a.qslot_bytes;
   const uint32_t qbar = q_empty_bar(bars, W, mine ? jc : 0);
-  const uint32_t rbar = r_empty_bar(bars, W, mine ? jc : 0);
-  int rn = 0, rdone = 0;                    // raw-row copies issued / known consumed
   uint32_t eparity = (1u << kStages) - 1;   // empty-barrier parity to wait for, per stage
   uint32_t used = 0, fpar = 0;              // stages ever filled; parity of their next fill
   int ps = 0, prev_seg = -1;
@@ -368,24 +357,9 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
     // chunk are only read on the next pass, after other lanes' work
     for (int pass = 0; pass < TQ_PRODUCER_PASSES && !done; ++pass) {
       const bool newq = n_n > 0 && n_seg != prev_seg;
-      // append: the newest position's tile is in this chunk (its block id in
-      // range) and the length was not cut: the raw K and V rows go into the
-      // query slot after the query rows (their own "taken" barrier)
-      bool app = false;
-      if constexpr (APPEND) {
-        const int app_i = n_len - 1 - n_t * kTileTokens >= 0 ? (n_len - 1 - n_t * kTileTokens) >> 4 : kChunk;
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i)
-          if (i == app_i) app = i < n_n && n_blk[i] >= 0 && n_blk[i] < a.num_blocks;
-        app = app && n_raw > 0 && n_raw == n_len;
-      }
       if (newq && qdone < qn) {   // the slot still holds rows the consumer has not taken
         if (!mbar_test(qbar, (qn - 1) & 1)) break;
         qdone = qn;
-      }
-      if (APPEND && app && rdone < rn) {    // the same for the raw rows
-        if (!mbar_test(rbar, (rn - 1) & 1)) break;
-        rdone = rn;
       }
       const uint32_t fb = full_bar(bars, jc, ps);
       if (!mbar_test(fb + 8, (eparity >> ps) & 1u)) break;
@@ -401,11 +375,10 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
           bytes += a.tile_bytes;
         }
       if (newq) bytes += a.qbuf_bytes;
-      if (APPEND && app) bytes += 2 * kRawRowBytes;
       sts128(sa + a.desc_off, make_uint4(static_cast<uint32_t>(n_seg), static_cast<uint32_t>(n_t << 4),
                                          static_cast<uint32_t>(n_len),
                                          static_cast<uint32_t>(n_n) | (okm << 4) | (last ? 256u : 0u) |
-                                             (newq ? 512u : 0u) | (APPEND && app ? kAppendBit : 0u)));
+                                             (newq ? 512u : 0u)));
       // No proxy fence: the consumer's reads of the stage are ordered before
       // these copies by its arrive on the empty barrier (release) and the
       // test above (acquire); the descriptor goes generic store -> generic load
@@ -419,19 +392,12 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
                                    static_cast<uint32_t>(a.tile_bytes);
           bulk_g2s(sa + i * a.tile_bytes, src, a.tile_bytes, fb, policy);
         }
-      if (APPEND && app) {
-        const long long row = (static_cast<long long>(n_b) * a.n_kv + n_h) * kRawRowBytes;
-        const uint32_t dst = qslot + static_cast<uint32_t>(a.qbuf_bytes);
-        bulk_g2s_plain(dst, static_cast<const uint8_t*>(a.new_k) + row, kRawRowBytes, fb);
-        bulk_g2s_plain(dst + kRawRowBytes, static_cast<const uint8_t*>(a.new_v) + row, kRawRowBytes, fb);
-      }
       if (newq) {
         const uint8_t* src = static_cast<const uint8_t*>(a.q) +
                              (static_cast<long long>(n_b) * a.n_q + n_h * a.group) * (kD * 2);
         bulk_g2s_plain(qslot, src, a.qbuf_bytes, fb);
         ++qn;
       }
-      if (APPEND && app) ++rn;
       if (n_n > 0) prev_seg = n_seg;
       used |= 1u << ps;
       fpar ^= 1u << ps;
@@ -461,13 +427,13 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
 // ---------------------------------------------------------------- append
 
 // The newest token of the stage's segment (position len - 1, in tile i of the
-// stage, row r): the warp quantises its raw key and value rows (in the query
-// slot at `raw`; the key in the first half, the value in the second) with the
-// store's arithmetic, writes
-// the bytes into the cache tile in global memory and patches the same row of
-// the stage's copy, which the bulk copy brought with the row's old bytes. The
-// patch goes through the generic proxy; the fence orders it before the
-// stage's next bulk fill (async proxy) once the consumer releases the stage.
+// stage, row r): the warp quantises its raw key and value rows (prefetched
+// into the query slot's tail at `raw`; the key in the first half-warp, the
+// value in the second) with the store's arithmetic, writes the bytes into the
+// cache tile in global memory and patches the same row of the stage's copy,
+// which the bulk copy brought with the row's old bytes. The patch goes
+// through the generic proxy; the fence orders it before the stage's next
+// bulk fill (async proxy) once the consumer releases the stage.
 template <int KMODE, int VBITS, typename TQ>
 __device__ __forceinline__ void append_newest(const DecodeArgs& a, uint32_t sa, uint4 desc, int lane, uint32_t raw,
                                            uint32_t codebook) {
@@ -476,7 +442,7 @@ __device__ __forceinline__ void append_newest(const DecodeArgs& a, uint32_t sa, 
   const int i = (p - tok0) >> 4, r = p & (kTileTokens - 1);
   const int bh = static_cast<int>(desc.x) / a.num_parts;
   const int b = bh / a.n_kv, h = bh - b * a.n_kv;
-  // the producer found this block id in range; its load overlaps the quantisation
+  // the tile was found, so this block id is in range; its load overlaps the quantisation
   const long long blk = ld_dep_s32(a.block_table + static_cast<long long>(b) * a.bt_stride + (p >> a.log2_bs));
   const int l = lane & 15;
   const TileGeom g = {a.k_off, a.k_row, a.v_off, a.v_row, a.knorm_off, a.vscale_off, a.vzero_off};
@@ -879,6 +845,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
 
   int cs = 0;
   bool aborted = false;
+  uint32_t rbuf = 0;   // append: offset of the current segment's raw rows in the slot's tail (two halves)
   for (;;) {
     const uint32_t fb = full_bar(bars, j, cs);
     if (!mbar_wait(fb, (fpar >> cs) & 1u)) { aborted = true; break; }
@@ -898,15 +865,37 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
         __syncwarp();   // every lane has read the query slot: the producer may refill it
         if (lane == 0) mbar_arrive(q_empty_bar(bars, W, j));
         c_seg = seg;
+        if constexpr (APPEND) {
+          // the segment's newest key and value rows, in case its last tile is
+          // in this warp's range: one 16-byte cp.async per lane into the half
+          // of the slot's tail this segment uses (the other half may still be
+          // the previous segment's, in flight)
+          rbuf ^= kRawRowBytes * 2;
+          const long long row = static_cast<long long>(seg / a.num_parts) * kRawRowBytes + 16 * (lane & 15);
+          const uint8_t* src = static_cast<const uint8_t*>(lane < 16 ? a.new_k : a.new_v) + row;
+          const uint32_t dst = qslots + static_cast<uint32_t>(j) * a.qslot_bytes + static_cast<uint32_t>(a.qbuf_bytes) +
+                               rbuf + (lane < 16 ? 0u : kRawRowBytes) + 16u * static_cast<uint32_t>(lane & 15);
+          asm volatile("cp.async.wait_group 1;\n" ::: "memory");   // the other half's copy has landed
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+          asm volatile("cp.async.commit_group;\n" ::: "memory");
+        }
       }
       const int tok0 = static_cast<int>(desc.y), len = static_cast<int>(desc.z);
       if (okm != (1u << n) - 1 && lane == 0) flag(a.status, TQ_DEV_BLOCK_OUT_OF_RANGE);
       if constexpr (APPEND) {
-        if (desc.w & kAppendBit) {
-          const uint32_t slot = qslots + static_cast<uint32_t>(j) * a.qslot_bytes;
-          append_newest<KMODE, VBITS, TQ>(a, sa, desc, lane, slot + static_cast<uint32_t>(a.qbuf_bytes),
-                                          bars + kCodebookOff);
-          if (lane == 0) mbar_arrive(r_empty_bar(bars, W, j));   // append_newest ends with __syncwarp
+        // the newest position of the segment is in this chunk (a chunk never
+        // passes the sequence's end, so reaching it is enough), its tile was
+        // found, and the length was not cut (only a length at the limit needs
+        // the raw value)
+        if (tok0 + kTileTokens * n >= len && ((okm >> (n - 1)) & 1u)) {
+          const int bh = seg / a.num_parts;
+          if (len < min(a.max_seq_len, a.cap) || ld_dep_s32(a.seq_lens + bh / a.n_kv) == len) {
+            asm volatile("cp.async.wait_all;\n" ::: "memory");
+            __syncwarp();   // every lane's rows have landed
+            const uint32_t raw = qslots + static_cast<uint32_t>(j) * a.qslot_bytes +
+                                 static_cast<uint32_t>(a.qbuf_bytes) + rbuf;
+            append_newest<KMODE, VBITS, TQ>(a, sa, desc, lane, raw, bars + kCodebookOff);
+          }
         }
       }
       int nv[kChunk];
@@ -934,6 +923,7 @@ __device__ void consumer_warp(const DecodeArgs& a, int W, int j, uint32_t bars, 
   } else if (c_seg >= 0) {
     finalize(c_seg);
   }
+  if constexpr (APPEND) asm volatile("cp.async.wait_all;\n" ::: "memory");   // no copy outlives the CTA
 }
 
 // ---------------------------------------------------------------- split kernel
@@ -969,12 +959,12 @@ split_kernel(const DecodeArgs a) {
   if (warp < kProducers) {
     if (warp == 0) {
       const int lane = threadIdx.x & 31;
-      for (int i = lane; i < 2 * W * kStages + (APPEND ? 2 : 1) * W; i += 32) mbar_init(bars + 8 * i, 1);
+      for (int i = lane; i < 2 * W * kStages + W; i += 32) mbar_init(bars + 8 * i, 1);
       asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (kProducers > 1) asm volatile("bar.sync 2, %0;\n" ::"r"(kProducers * 32) : "memory");   // barriers exist
     else __syncwarp();
-    producer_warp<APPEND>(a, W, warp, bars, qslots, first, lut, kLut);   // waits for the previous kernel itself
+    producer_warp(a, W, warp, bars, qslots, first, lut, kLut);   // waits for the previous kernel itself
   } else {
     constexpr int kP = kProducers * 32;
     if constexpr (kLut != 0) build_lut<KMODE>(lut, a.cent, threadIdx.x - kP, blockDim.x - kP);
@@ -1375,7 +1365,7 @@ bool launch_shape(int tile_bytes, int group, bool append, LaunchShape* s) {
   s->stage_bytes = (s->desc_off + 16 + 127) & ~127;
   const uint32_t klut = lut_bytes<KMODE>();
   // the window may start at 0 or after a small reserved area; take the worse
-  const uint32_t qbytes = static_cast<uint32_t>(group) * kD * 2 + (append ? 2 * kRawRowBytes : 0u);
+  const uint32_t qbytes = static_cast<uint32_t>(group) * kD * 2 + (append ? 4 * kRawRowBytes : 0u);
   s->qslot_bytes = static_cast<int>(qbytes);
   int w = consumers_that_fit(0, optin, klut, s->stage_bytes, qbytes);
   const int w2 = consumers_that_fit(1024, optin, klut, s->stage_bytes, qbytes);

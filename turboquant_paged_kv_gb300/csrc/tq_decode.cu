@@ -1172,6 +1172,98 @@ __global__ void __launch_bounds__(8 * kD) reduce_bh_kernel(const ReduceArgs a) {
   store_out<TO>(a.out, orow * kD + d, den > 0.f ? acc / den : 0.f);
 }
 
+// Stream-K records (one partition per sequence), many (sequence, KV head)
+// pairs: one CTA per pair, thread (gg, d) = query head gg of the group,
+// coordinate d. A pair's tiles [seq0, seq0 + nt) of the line were split
+// over a contiguous warp range, the owners of its first and last tile, so
+// every thread finds its candidates by two divisions: no enumeration, no
+// shared memory, no barrier. Each warp scans the lengths itself (before the
+// dependency wait when the launch follows the split kernel); each thread
+// then issues the loads of 8 candidates' LSEs and coordinates at once and
+// merges them online.
+__device__ __forceinline__ void prefix_all(const ReduceArgs& a, int b, int lane, long long* before, long long* total,
+                                           int* len) {
+  long long bf = 0, tt = 0;
+  int ln = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    const int j = b0 + lane;
+    const int len_j = j < a.batch ? reduce_len(a, j) : 0;
+    if (b0 == (b & ~31)) ln = __shfl_sync(0xffffffffu, len_j, b & 31);
+    long long nt = (len_j + kTileTokens - 1) / kTileTokens;
+    long long nb = j < b ? nt : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      nt += __shfl_xor_sync(0xffffffffu, nt, o);
+      nb += __shfl_xor_sync(0xffffffffu, nb, o);
+    }
+    tt += nt;
+    bf += nb;
+  }
+  *before = bf * a.n_kv;
+  *total = tt * a.n_kv;
+  *len = ln;
+}
+
+template <typename TO>
+__global__ void __launch_bounds__(8 * kD) reduce_sk_kernel(const ReduceArgs a) {
+  constexpr int kCand = 8;
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int G = a.group;
+  const int gg = threadIdx.x / kD, d = threadIdx.x - gg * kD;
+  const int lane = threadIdx.x & 31;
+  if (!a.early_lens) {
+    grid_dep_wait();
+    grid_dep_launch();
+  }
+  long long before, T;
+  int len;
+  prefix_all(a, b, lane, &before, &T, &len);
+  const long long orow = static_cast<long long>(b) * a.n_q + static_cast<long long>(h) * G + gg;
+  const int nt = (len + kTileTokens - 1) / kTileTokens;
+  const long long nw = a.num_warps;
+  const bool narrow = (T + 1) * nw < (1ll << 32);
+  const long long seq0 = before + static_cast<long long>(h) * nt;
+  // owners of the pair's first and last tile (len > 0, so T > 0)
+  const long long wf = len > 0 ? div_nw((seq0 + 1) * nw - 1, T, narrow) : 0;
+  const long long wl = len > 0 ? div_nw((seq0 + nt) * nw - 1, T, narrow) : -1;
+  const bool all_own = T >= nw;   // every warp owns a tile: no candidate to drop
+  const long long seg = static_cast<long long>(b) * a.n_kv + h;   // record of warp w: seg + w
+  if (a.early_lens) {
+    grid_dep_wait();   // the records come from the split kernel
+    grid_dep_launch();
+  }
+  if (len <= 0) {
+    store_out<TO>(a.out, orow * kD + d, 0.f);
+    return;
+  }
+  float m = -INFINITY, acc = 0.f, den = 0.f;
+  for (long long w0 = wf; w0 <= wl; w0 += kCand) {
+    float lse[kCand], x[kCand];
+#pragma unroll
+    for (int i = 0; i < kCand; ++i) {
+      const long long w = w0 + i;
+      const bool ok = w <= wl && (all_own || warp_owns_tiles(w, T, nw, narrow));
+      const long long rec = seg + w;
+      lse[i] = ok ? ld_dep_f32(a.rec_lse + rec * G + gg) : -INFINITY;
+      x[i] = ok ? ld_dep_f32(a.rec_o + (rec * G + gg) * kD + d) : 0.f;
+    }
+    float cm = m;
+#pragma unroll
+    for (int i = 0; i < kCand; ++i) cm = fmaxf(cm, lse[i]);
+    if (cm == -INFINITY) continue;
+    const float al = m == -INFINITY ? 0.f : exp2f(m - cm);
+    acc *= al;
+    den *= al;
+#pragma unroll
+    for (int i = 0; i < kCand; ++i) {
+      const float wgt = lse[i] == -INFINITY ? 0.f : exp2f(lse[i] - cm);
+      den += wgt;
+      acc = wgt != 0.f ? fmaf(wgt, x[i], acc) : acc;
+    }
+    m = cm;
+  }
+  store_out<TO>(a.out, orow * kD + d, den > 0.f ? acc / den : 0.f);
+}
+
 // Few pairs with many partials each: one CTA per (sequence, query head), 4
 // warps; thread d of 128 = coordinate d in the final merge. Every warp scans
 // the partitions 32 at a time; the (partition, warp) candidates of a group,
@@ -1542,6 +1634,13 @@ tq_status run_reduce(const tq_config* cfg, const int* seq_lens, int batch, int m
     if (out_dtype == TQ_DTYPE_F32) err = launch_pdl(reduce_qh_kernel<float>, grid, block, 0, stream, r);
     else if (out_dtype == TQ_DTYPE_F16) err = launch_pdl(reduce_qh_kernel<__half>, grid, block, 0, stream, r);
     else err = launch_pdl(reduce_qh_kernel<__nv_bfloat16>, grid, block, 0, stream, r);
+  } else if (P.part_tiles == 0) {
+    // stream-K: each pair's records are one contiguous warp range
+    const dim3 grid(static_cast<unsigned>(cfg->num_kv_heads), static_cast<unsigned>(batch));
+    const dim3 block(static_cast<unsigned>(G * kD));
+    if (out_dtype == TQ_DTYPE_F32) err = launch_pdl(reduce_sk_kernel<float>, grid, block, 0, stream, r);
+    else if (out_dtype == TQ_DTYPE_F16) err = launch_pdl(reduce_sk_kernel<__half>, grid, block, 0, stream, r);
+    else err = launch_pdl(reduce_sk_kernel<__nv_bfloat16>, grid, block, 0, stream, r);
   } else {
     const dim3 grid(static_cast<unsigned>(cfg->num_kv_heads), static_cast<unsigned>(batch));
     const dim3 block(static_cast<unsigned>(G * kD));

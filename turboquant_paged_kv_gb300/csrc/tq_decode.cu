@@ -435,7 +435,7 @@ __device__ void producer_warp(const DecodeArgs& a, int W, int p, uint32_t bars, 
 // through the generic proxy; the fence orders it before the stage's next
 // bulk fill (async proxy) once the consumer releases the stage.
 template <int KMODE, int VBITS, typename TQ>
-__device__ __forceinline__ void append_newest(const DecodeArgs& a, uint32_t sa, uint4 desc, int lane, uint32_t raw,
+__device__ __noinline__ void append_newest(const DecodeArgs& a, uint32_t sa, uint4 desc, int lane, uint32_t raw,
                                            uint32_t codebook) {
   const int len = static_cast<int>(desc.z), tok0 = static_cast<int>(desc.y);
   const int p = len - 1;

@@ -826,7 +826,6 @@ for _ in range({steps}):
 print(json.dumps({{"times": times}}))
 """
 PROD_ORACLE_TOKENS = 4096
-TF32_PER_BF16 = 1.1 / 2.25   # nominal dense tf32 / bf16 tensor rates of the part
 
 
 def run_prod(args):
@@ -836,7 +835,8 @@ def run_prod(args):
     (a query-prep launch and the scores launch); four copies of the 54.5 MB
     cache are rotated so no step finds its keys in L2. The line also carries
     tq_prod_store of an 8192-token bf16 prefill chunk (its contraction, the
-    projection S r, runs on TF32 tensor cores) and the oracle's prod_scores
+    projection S r, runs on tensor cores with fp16 hi/lo operands) and the
+    oracle's prod_scores
     on one whole sequence
     (4096 positions). Prints one JSON line of its own."""
     import torch
@@ -896,7 +896,6 @@ def run_prod(args):
     gbs = nbytes / (ms * 1e-3) / 1e9
     store_tflops = STORE_TOKENS * w.n_kv * 2 * w.d * w.d / (ms_store * 1e-3) / 1e12
     tpeak, tpeak_src = _tensor_peak()
-    tf32_peak = tpeak * TF32_PER_BF16
     line = {
         "op": "prod", "metric": "TurboQuant_prod scores GB/s (packed prod keys read + fp32 scores written); keys/s",
         "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": reps, "warmup": args.warmup, "ms_per_step": ms,
@@ -911,9 +910,9 @@ def run_prod(args):
                      "traffic": _profile_field("tq_prod.cu", "prod_scores_prod.md", "dram_bytes_per_launch")},
         "store": {"kernel": "prod_store_kernel (tq_prod_store)", "tokens": STORE_TOKENS,
                   "mtok_s": STORE_TOKENS / (ms_store * 1e-3) / 1e6, "ms_per_launch": ms_store,
-                  "roofline": {"bound": "tensor", "achieved": store_tflops, "peak": tf32_peak,
-                               "unit": "TFLOP/s", "frac": store_tflops / tf32_peak,
-                               "peak_source": tpeak_src + " x %.3f (nominal tf32 / bf16 dense ratio)" % TF32_PER_BF16,
+                  "roofline": {"bound": "tensor", "achieved": store_tflops, "peak": tpeak,
+                               "unit": "TFLOP/s", "frac": store_tflops / tpeak,
+                               "peak_source": tpeak_src + " (the projection runs on f16 operands, bf16's rate)",
                                "flops_per_launch": STORE_TOKENS * w.n_kv * 2 * w.d * w.d,
                                "traffic": _profile_field("tq_prod_store.cu", "prod_store_prod.md",
                                                          "dram_bytes_per_launch")}},

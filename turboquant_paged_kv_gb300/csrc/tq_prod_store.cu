@@ -12,14 +12,16 @@
 // <S y, signs>.
 //
 // GB300 design:
-//   store   one CTA per SM loops over groups of 128 vectors. Each thread
-//           issues all of a group's key and slot loads at once (the next
-//           group's go out while the current one is projected). A half-warp
-//           per vector rotates and quantises (as tq_store does) and leaves the
-//           residual r in shared memory; then each warp computes S r for 16
-//           vectors on tensor cores (mma.sync TF32, three products of hi/lo
-//           splits, so the result carries fp32 accuracy) and packs the signs
-//           with warp ballots.
+//   store   two CTAs per SM (105 KB of shared memory, 128 registers each)
+//           loop over groups of 64 vectors. Each thread issues all of a
+//           group's key and slot loads at once (the next group's go out while
+//           the current one is projected). A half-warp per vector rotates and
+//           quantises (as tq_store does) and leaves the residual, scaled by
+//           2^6, in shared memory as fp16 hi and lo parts; then each warp
+//           computes 64 rows of S r for 16 vectors on tensor cores (mma.sync
+//           m16n8k16 f16, three products of the hi/lo splits, f32 sums: the
+//           result carries fp32 accuracy) and packs the signs with warp
+//           ballots.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -37,31 +39,31 @@
 namespace tq {
 namespace {
 
-constexpr int kGroupVecs = 128;              // vectors per CTA pass of the store
+constexpr int kGroupVecs = 64;               // vectors per CTA pass of the store
+constexpr int kCtasPerSm = 2;
 
-// TF32 (10-bit mantissa) rounding of x, round to nearest, ties away (cvt.rna).
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
-  return r;
+// x = hi + lo with hi, lo fp16 (hi = fp16(x), lo = fp16(x - hi)): the three
+// products hi*hi + hi*lo + lo*hi of two such pairs give the product to about
+// 2^-21 relative, fp32's accuracy, as long as the lo parts stay normal (the
+// residuals are scaled by 2^6 for that; S is N(0, 1)).
+__device__ __forceinline__ void split_h2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+  const __half l0 = __float2half_rn(x0 - __half2float(h0)), l1 = __float2half_rn(x1 - __half2float(h1));
+  hi = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+  lo = static_cast<uint32_t>(__half_as_ushort(l0)) | (static_cast<uint32_t>(__half_as_ushort(l1)) << 16);
 }
 
-// x = hi + lo with hi, lo TF32: the three products hi*hi + hi*lo + lo*hi of
-// two such pairs give the fp32 product to ~2^-21 relative.
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = to_tf32(x);
-  lo = to_tf32(x - __uint_as_float(hi));
-}
-
-__device__ __forceinline__ void mma_tf32(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+__device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Row stride (floats) of the shared S and R tables: 136 = 8 mod 32, so the
-// 8-byte operand loads of a half-warp (rows g, columns 2 t) are conflict-free.
+// Row stride (halves) of the shared S and R tables: 136 halves = 68 words =
+// 4 mod 32, so the 4-byte operand loads of a warp (rows g, words t) hit 32
+// different banks.
 constexpr int kPad = 136;
+constexpr float kResidualScale = 64.f;   // exact; scales S r by 2^6, so no sign changes
 
 struct ProdStoreArgs {
   const void* key;
@@ -76,10 +78,11 @@ struct ProdStoreArgs {
   float cent[4];
 };
 
-// Shared memory: S as TF32 hi and lo parts and the group's residuals R, each
-// [128][kPad] floats; the tile and row of each vector of the group (null
-// tile: nothing to write).
-constexpr size_t kStoreSmem = 3 * static_cast<size_t>(kD) * kPad * sizeof(float) +
+// Shared memory: S as fp16 hi and lo parts, [128][kPad] halves each; the
+// group's scaled residuals R as fp16 hi and lo parts, [64][kPad] halves each;
+// the tile and row of each vector of the group (null tile: nothing to write).
+// 105 KB: two CTAs per SM.
+constexpr size_t kStoreSmem = 2 * static_cast<size_t>(kD) * kPad * 2 + 2 * static_cast<size_t>(kGroupVecs) * kPad * 2 +
                               kGroupVecs * (sizeof(uint8_t*) + sizeof(int));
 
 // The inputs of one group for the thread (half-warp h = threadIdx.x / 16,
@@ -118,12 +121,13 @@ __device__ __forceinline__ void unpack8(const uint4 raw, float out[8]) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) prod_store_kernel(const ProdStoreArgs a) {
-  extern __shared__ __align__(16) float s_store[];
-  uint32_t* s_hi = reinterpret_cast<uint32_t*>(s_store);   // S[i][j] at i * kPad + j
-  uint32_t* s_lo = s_hi + kD * kPad;
-  float* R = s_store + 2 * kD * kPad;                       // R[v][j] at v * kPad + j
-  uint8_t** tiles = reinterpret_cast<uint8_t**>(R + kGroupVecs * kPad);
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) prod_store_kernel(const ProdStoreArgs a) {
+  extern __shared__ __align__(16) uint16_t s_store[];
+  uint16_t* s_hi = s_store;                   // S[i][j] at i * kPad + j (halves)
+  uint16_t* s_lo = s_hi + kD * kPad;
+  uint16_t* r_hi = s_lo + kD * kPad;          // 2^6 R[v][j] at v * kPad + j
+  uint16_t* r_lo = r_hi + kGroupVecs * kPad;
+  uint8_t** tiles = reinterpret_cast<uint8_t**>(r_lo + kGroupVecs * kPad);
   int* trow = reinterpret_cast<int*>(tiles + kGroupVecs);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, l = lane & 15, hv = threadIdx.x >> 4;
   const long long groups = (a.num_vectors + kGroupVecs - 1) / kGroupVecs;
@@ -142,9 +146,11 @@ __global__ void __launch_bounds__(kThreads, 1) prod_store_kernel(const ProdStore
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int e = 4 * (threadIdx.x + k * kThreads), i = e >> 7, j = e & (kD - 1);
-      const float x[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) split_tf32(x[q], s_hi[i * kPad + j + q], s_lo[i * kPad + j + q]);
+      uint32_t h01, l01, h23, l23;
+      split_h2(v[k].x, v[k].y, h01, l01);
+      split_h2(v[k].z, v[k].w, h23, l23);
+      *reinterpret_cast<uint2*>(s_hi + i * kPad + j) = make_uint2(h01, h23);
+      *reinterpret_cast<uint2*>(s_lo + i * kPad + j) = make_uint2(l01, l23);
     }
   }
   for (; grp < groups; grp += gridDim.x) {
@@ -198,9 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1) prod_store_kernel(const ProdStore
         rr = fmaf(res[j], res[j], rr);
       }
       rr = half_sum(rr);
-      float* rrow = R + gv * kPad + 8 * l;
-      *reinterpret_cast<float4*>(rrow) = make_float4(res[0], res[1], res[2], res[3]);
-      *reinterpret_cast<float4*>(rrow + 4) = make_float4(res[4], res[5], res[6], res[7]);
+      uint32_t rh[4], rl[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) split_h2(kResidualScale * res[2 * q], kResidualScale * res[2 * q + 1], rh[q], rl[q]);
+      *reinterpret_cast<uint4*>(r_hi + gv * kPad + 8 * l) = make_uint4(rh[0], rh[1], rh[2], rh[3]);
+      *reinterpret_cast<uint4*>(r_lo + gv * kPad + 8 * l) = make_uint4(rl[0], rl[1], rl[2], rl[3]);
       if (l == 0) {
         tiles[gv] = live ? tile : nullptr;
         trow[gv] = r;
@@ -217,44 +225,49 @@ __global__ void __launch_bounds__(kThreads, 1) prod_store_kernel(const ProdStore
     // the next group's loads are in flight during the projection
     if (grp + gridDim.x < groups) load_group<T>(a, grp + gridDim.x, hv, l, key, slot);
     __syncthreads();
-    // ---- phase 2: warp w projects vectors 16 w .. 16 w + 15 on tensor cores:
-    // P[v][i] = sum_j R[v][j] S[i][j], mma.sync m16n8k8 TF32 with A = R (rows
-    // v), B = S^T, three products per step (hi*hi + hi*lo + lo*hi). The k
-    // order inside a step is permuted so a lane's two operand values are
-    // adjacent (k slots t and t + 4 hold columns 2 t and 2 t + 1 of the step):
-    // A and B use the same order, so the sums are unchanged.
-    const int g = lane >> 2, t = lane & 3;
-    float acc[16][4];
+    // ---- phase 2: warp w projects vectors 16 vb .. 16 vb + 15 (vb = w % 4) onto
+    // rows 64 oh .. 64 oh + 63 of S (oh = w / 4) on tensor cores: 2^6 P[v][i] =
+    // sum_j 2^6 R[v][j] S[i][j], mma.sync m16n8k16 f16 with A = R (rows v),
+    // B = S^T, three products per step (hi*hi + hi*lo + lo*hi), f32 sums.
+    const int g = lane >> 2, t = lane & 3, vb = warp & 3, oh = warp >> 2;
+    float acc[8][4];
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    const float* Rw = R + warp * 16 * kPad;
-#pragma unroll 1
-    for (int k0 = 0; k0 < kD; k0 += 8) {
-      const float2 rg = *reinterpret_cast<const float2*>(Rw + g * kPad + k0 + 2 * t);
-      const float2 rh = *reinterpret_cast<const float2*>(Rw + (g + 8) * kPad + k0 + 2 * t);
-      uint32_t ah[4], al[4];   // (row g, slot t), (row g + 8, slot t), (row g, slot t + 4), (row g + 8, slot t + 4)
-      split_tf32(rg.x, ah[0], al[0]);
-      split_tf32(rh.x, ah[1], al[1]);
-      split_tf32(rg.y, ah[2], al[2]);
-      split_tf32(rh.y, ah[3], al[3]);
+    for (int nt = 0; nt < 8; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const uint16_t* rh0 = r_hi + (16 * vb + g) * kPad + 2 * t;
+    const uint16_t* rl0 = r_lo + (16 * vb + g) * kPad + 2 * t;
+    const uint16_t* sh0 = s_hi + (64 * oh + g) * kPad + 2 * t;
+    const uint16_t* sl0 = s_lo + (64 * oh + g) * kPad + 2 * t;
+#pragma unroll 2
+    for (int k0 = 0; k0 < kD; k0 += 16) {
+      uint32_t ah[4], al[4];   // (row g, k 2t), (row g + 8, k 2t), (row g, k 2t + 8), (row g + 8, k 2t + 8)
+      ah[0] = *reinterpret_cast<const uint32_t*>(rh0 + k0);
+      ah[1] = *reinterpret_cast<const uint32_t*>(rh0 + 8 * kPad + k0);
+      ah[2] = *reinterpret_cast<const uint32_t*>(rh0 + k0 + 8);
+      ah[3] = *reinterpret_cast<const uint32_t*>(rh0 + 8 * kPad + k0 + 8);
+      al[0] = *reinterpret_cast<const uint32_t*>(rl0 + k0);
+      al[1] = *reinterpret_cast<const uint32_t*>(rl0 + 8 * kPad + k0);
+      al[2] = *reinterpret_cast<const uint32_t*>(rl0 + k0 + 8);
+      al[3] = *reinterpret_cast<const uint32_t*>(rl0 + 8 * kPad + k0 + 8);
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int n = 8 * nt + g;   // B column: output row i = n of S
-        const uint2 bh = *reinterpret_cast<const uint2*>(s_hi + n * kPad + k0 + 2 * t);
-        const uint2 bl = *reinterpret_cast<const uint2*>(s_lo + n * kPad + k0 + 2 * t);
-        mma_tf32(acc[nt], ah, bh.x, bh.y);
-        mma_tf32(acc[nt], ah, bl.x, bl.y);
-        mma_tf32(acc[nt], al, bh.x, bh.y);
+      for (int nt = 0; nt < 8; ++nt) {   // B column n = 64 oh + 8 nt + g: row n of S
+        const uint32_t bh0 = *reinterpret_cast<const uint32_t*>(sh0 + 8 * nt * kPad + k0);
+        const uint32_t bh1 = *reinterpret_cast<const uint32_t*>(sh0 + 8 * nt * kPad + k0 + 8);
+        const uint32_t bl0 = *reinterpret_cast<const uint32_t*>(sl0 + 8 * nt * kPad + k0);
+        const uint32_t bl1 = *reinterpret_cast<const uint32_t*>(sl0 + 8 * nt * kPad + k0 + 8);
+        mma_f16(acc[nt], ah, bh0, bh1);
+        mma_f16(acc[nt], ah, bl0, bl1);
+        mma_f16(acc[nt], al, bh0, bh1);
       }
     }
-    // signs: acc[nt][e] is P[16 w + g + 8 (e >> 1)][8 nt + 2 t + (e & 1)]. The
-    // ballot of (nt, e) gives bit 4 g' + t' = the sign of output 8 nt + 2 t' +
-    // (e & 1) of vector g' (+ 8): one byte of a vector's stream per (nt, half)
-    // from the two parities. Lane (g, t) assembles bytes nt = 4 t .. 4 t + 3 of
-    // vectors 16 w + g and 16 w + g + 8, i.e. word t of their 128-bit streams.
+    // signs: acc[nt][e] is 2^6 P[16 vb + g + 8 (e >> 1)][64 oh + 8 nt + 2 t +
+    // (e & 1)]. The ballot of (nt, e) gives bit 4 g' + t' = the sign of output
+    // 64 oh + 8 nt + 2 t' + (e & 1) of vector g' (+ 8): byte 8 oh + nt of a
+    // vector's stream per (nt, half) from the two parities. Lane (g, t < 2)
+    // assembles bytes nt = 4 t .. 4 t + 3 of vectors 16 vb + g and 16 vb + g +
+    // 8, i.e. word 2 oh + t of their 128-bit streams.
     uint32_t word[2] = {0u, 0u};
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
+    for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const uint32_t m0 = __ballot_sync(0xffffffffu, acc[nt][2 * hf] >= 0.f);
@@ -268,11 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1) prod_store_kernel(const ProdStore
         }
       }
     }
+    if (t < 2) {
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int gv = warp * 16 + g + 8 * hf;
-      uint8_t* tile = tiles[gv];
-      if (tile) *reinterpret_cast<uint32_t*>(tile + kSOff + trow[gv] * kSRow + 4 * t) = word[hf];
+      for (int hf = 0; hf < 2; ++hf) {
+        const int gv = 16 * vb + g + 8 * hf;
+        uint8_t* tile = tiles[gv];
+        if (tile) *reinterpret_cast<uint32_t*>(tile + kSOff + trow[gv] * kSRow + 4 * (2 * oh + t)) = word[hf];
+      }
     }
     __syncthreads();   // R and tiles are rewritten by the next group
   }
@@ -324,7 +339,8 @@ tq_status tq_prod_store(const tq_config* cfg, const tq_codebook* cb, const float
   const int sms = sm_count();
   if (sms <= 0) return TQ_ERR_CUDA;
   const long long groups = (vectors + kGroupVecs - 1) / kGroupVecs;
-  const unsigned grid = static_cast<unsigned>(groups < sms ? groups : sms);
+  const long long resident = static_cast<long long>(kCtasPerSm) * sms;
+  const unsigned grid = static_cast<unsigned>(groups < resident ? groups : resident);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err;
   if (in_dtype == TQ_DTYPE_BF16) {
